@@ -1,0 +1,207 @@
+/*
+ * usp.h — C ABI of libusp_gb300.so: context-parallel exact softmax attention with all
+ * sequence chunks ("virtual ranks") on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (web pages on context parallelism):
+ *   [UAA]   diffusers issue #12706, "UAA: Ulysses Anything Attention" — Ulysses with arbitrary
+ *           per-rank sequence lengths, no padding, per-rank seq_len gathered on the host.
+ *   [CP]    Hugging Face diffusers docs, "Context parallelism" — sections Ring Attention,
+ *           Ulysses Attention, Unified Attention, Ulysses Anything Attention, Ring Anything.
+ *   [USP]   diffusers PR #12693, "Add Unified Sequence Parallel attention" — the ring step's
+ *           (out, lse) merge and the lse layout (B, S, H_LOCAL).
+ *   [YC]    sourcepulse summary of USP / yunchang, "Highlighted Details" — ring orderings
+ *           "basic" (contiguous), "zigzag" and "stripe".
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense, row-major.  Q, K, V, O are [B][S][H][D]; the log-sum-exp (LSE) is fp32
+ *     [B][S][H], natural log, softmax scale included ([USP]: "the lse is of shape
+ *     (B, S, H_LOCAL)").
+ *   - All pointers named src/dst/q/k/v/o/lse/workspace/status are DEVICE pointers owned by the
+ *     caller.  seq_lens, head_counts and usp_positions_t are HOST memory, read during the call
+ *     only ([UAA]: the per-rank lengths travel on the host, which avoids forced device syncs).
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream) and never
+ *     synchronises the host with the device, except usp_check_status.
+ *   - The library allocates no device memory and keeps no global state; calls on different
+ *     streams are independent if their buffers are.
+ *   - Errors are return codes; usp_last_error() gives a thread-local message for the last
+ *     failing call of the calling thread.  On any error nothing has been launched.
+ *   - Head dimension D must be 64 or 128 for attention; re-layout accepts any D >= 1.
+ */
+#ifndef USP_GB300_H
+#define USP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (declared here without including the CUDA headers). */
+typedef struct CUstream_st* usp_stream_t;
+
+typedef enum usp_status {
+  USP_OK = 0,
+  USP_ERR_INVALID_ARG = 1, /* bad size, split, pointer alignment or NULL pointer */
+  USP_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. D = 96) */
+  USP_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed (launch, tensor-map encode) */
+  USP_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (from usp_check_status) */
+  USP_ERR_WORKSPACE = 5,   /* workspace NULL, misaligned or smaller than required */
+  USP_ERR_NO_DEVICE = 6    /* the current device is not an sm_103 GPU */
+} usp_status_t;
+
+typedef enum usp_dtype { USP_BF16 = 0, USP_FP32 = 1 } usp_dtype_t;
+
+/* Ring chunk ordering [YC].  Readings (the pages name them without a definition):
+ *   CONTIGUOUS: ring rank r holds piece r of the default split of S into R pieces.
+ *   ZIGZAG:     split S into 2R pieces (default split); rank r holds piece r then piece 2R-1-r.
+ *   STRIPE:     token t goes to rank t mod R, local index t / R.
+ * Default split of n items into P parts: part p has floor(n/P) + (p < n mod P) items. */
+typedef enum usp_order {
+  USP_ORDER_CONTIGUOUS = 0,
+  USP_ORDER_ZIGZAG = 1,
+  USP_ORDER_STRIPE = 2
+} usp_order_t;
+
+/* Global token positions of a chunk's rows, used by the causal mask: row i of the chunk has
+ * position start[0] + i*stride for i < len[0], else start[1] + (i - len[0])*stride.
+ * n_seg is 1 or 2.  Positions must increase with the row index.  This covers a contiguous chunk
+ * (1 segment, stride 1), a zigzag chunk (2 segments) and a stripe chunk (stride R). */
+typedef struct usp_positions {
+  int32_t n_seg;
+  int32_t start[2];
+  int32_t len[2];
+  int32_t stride;
+} usp_positions_t;
+
+/* ---------------------------------------------------------------------------------------------
+ * usp_relayout_seq2head — the first Ulysses all-to-all as a local permutation.
+ * [CP] Ulysses Attention: the first all-to-all regroups the data so that each rank holds every
+ * token for a subset of heads.  [UAA]: per-rank lengths are arbitrary and nothing is padded.
+ *
+ *   src: P sequence chunks back to back; chunk q is [B][seq_lens[q]][H][D].
+ *   dst: P head-sharded buffers back to back; buffer p is [B][S][head_counts[p]][D] with
+ *        S = sum(seq_lens), and dst_p[b][o_q + t][h][d] = src_q[b][t][g_p + h][d] where
+ *        o_q = sum of seq_lens before q and g_p = sum of head_counts before p.
+ *   dt: element type (2-byte BF16 or 4-byte FP32; the copy is bit-exact either way).
+ *   seq_lens: host int32[P], each >= 0.  head_counts: host int32[P], each >= 1, summing to H, or
+ *   NULL for the default split of H over P (ranks may then hold different head counts: [CP]
+ *   Ulysses Anything Attention removes the head-divisibility requirement).
+ *   1 <= P <= 64.  src and dst must not overlap.
+ *   Errors: INVALID_ARG for P out of range, B/H/D < 1, a negative length, head counts not
+ *   summing to H, H < P with head_counts NULL, NULL buffers.
+ * ------------------------------------------------------------------------------------------- */
+usp_status_t usp_relayout_seq2head(const void* src, void* dst, usp_dtype_t dt, int B, int H, int D,
+                                   int P, const int32_t* seq_lens, const int32_t* head_counts,
+                                   usp_stream_t stream);
+
+/* usp_relayout_head2seq — the second Ulysses all-to-all, the exact inverse of seq2head: src is
+ * the P head-sharded buffers, dst the P sequence chunks (same layouts and arguments as above).
+ * [CP] Ulysses Attention: a second all-to-all regroups the results by token; [USP] sends the
+ * lse through the same exchange (use dt = USP_FP32 and D = 1 for an LSE [B][S][H]). */
+usp_status_t usp_relayout_head2seq(const void* src, void* dst, usp_dtype_t dt, int B, int H, int D,
+                                   int P, const int32_t* seq_lens, const int32_t* head_counts,
+                                   usp_stream_t stream);
+
+/* usp_reorder — global sequence <-> ring-rank chunks under an ordering [YC].
+ *   inverse = 0: src is global [B][S][H][D]; dst is R chunks back to back, chunk r is
+ *                [B][s_r][H][D] holding rank r's tokens in local order (see usp_order_t).
+ *   inverse = 1: the reverse copy.
+ *   Bit-exact.  1 <= R <= 64.  Errors: INVALID_ARG for R out of range, S < 0, B/H/D < 1, NULL
+ *   buffers. */
+usp_status_t usp_reorder(const void* src, void* dst, usp_dtype_t dt, int B, int S, int H, int D,
+                         int R, usp_order_t order, int inverse, usp_stream_t stream);
+
+/* usp_attn_partial — one ring step: exact attention of one Q chunk against one K/V chunk,
+ * returning the partial output and its log-sum-exp ([USP]: the backend returns "out, lse";
+ * [CP] Ring Attention: each rank attends to the K/V block it holds).
+ *
+ *   q: bf16, B*Sq rows of q_row_stride elements (batch-major: row b*Sq + i), head h of a row at
+ *      element h*D.  k, v: bf16, B*Sk rows of kv_row_stride elements, same head layout.
+ *      Row strides are in elements, >= H*D, and row_stride*2 must be a multiple of 16 bytes;
+ *      q, k, v must be 16-byte aligned.
+ *   scale: softmax scale (1/sqrt(D) for standard attention).
+ *   q_pos, k_pos: host descriptions of the chunks' global positions; both NULL = non-causal.
+ *      Causal: key j visible to query i iff kpos(j) <= qpos(i) (diagonal included).
+ *   o: [B][Sq][H][D] of o_dt (USP_FP32 for a partial; USP_BF16 allowed), 16-byte aligned.
+ *   lse: fp32 [B][Sq][H]; a query that sees no key gets o = 0 and lse = -inf.
+ *   status: device uint32 the kernel ORs error bits into (bounded waits), or NULL.
+ *   Errors: INVALID_ARG (sizes, alignment, positions not increasing, only one of q_pos/k_pos),
+ *   UNSUPPORTED (D not 64 or 128), CUDA (tensor-map encode or launch failure). */
+usp_status_t usp_attn_partial(const void* q, const void* k, const void* v, int B, int H, int Sq,
+                              int Sk, int D, int64_t q_row_stride, int64_t kv_row_stride,
+                              float scale, const usp_positions_t* q_pos,
+                              const usp_positions_t* k_pos, void* o, usp_dtype_t o_dt, float* lse,
+                              uint32_t* status, usp_stream_t stream);
+
+/* usp_lse_merge — the ring step's LSE-weighted combine over n_parts partials ([USP]:
+ * out = prev_out - sigmoid(lse - prev_lse) * (prev_out - out),
+ * lse = prev_lse - logsigmoid(prev_lse - lse), in fp32).  This kernel merges all partials of a
+ * row in one pass with the equivalent max-shifted form (exact in real arithmetic):
+ * m = max_k lse_k, w_k = exp(lse_k - m), out = sum_k w_k out_k / sum_k w_k,
+ * lse = m + ln sum_k w_k.  Partials with lse = -inf contribute nothing and their out is not read;
+ * a row whose partials are all -inf gets out = 0, lse = -inf.
+ *
+ *   o_parts: fp32, part k at o_parts + k*o_part_stride (elements), each [n_rows][H][D].
+ *   lse_parts: fp32, part k at lse_parts + k*lse_part_stride, each [n_rows][H].
+ *   o_out: [n_rows][H][D] of out_dt; lse_out: fp32 [n_rows][H] (may be NULL).
+ *   1 <= n_parts <= 16; D a multiple of 4 and <= 256; 16-byte aligned o pointers and strides.
+ *   Errors: INVALID_ARG otherwise. */
+usp_status_t usp_lse_merge(int n_parts, const float* o_parts, int64_t o_part_stride,
+                           const float* lse_parts, int64_t lse_part_stride, int64_t n_rows, int H,
+                           int D, void* o_out, usp_dtype_t out_dt, float* lse_out,
+                           usp_stream_t stream);
+
+/* usp_attention — the whole method end to end on one GPU ([CP] Unified Attention: an all-to-all
+ * inside each Ulysses group, Ring Attention on the result, the reverse all-to-all; with
+ * ulysses_degree = 1 it is Ring Attention, with ring_degree = 1 Ulysses (Anything) Attention).
+ *
+ *   q, k, v: bf16 global [B][S][H][D] (16-byte aligned).  Virtual rank c = r*ulysses_degree + u
+ *   (ring group r, Ulysses index u) holds rows [o, o + seq_lens[c]) of ring chunk r, whose tokens
+ *   the ordering fixes; seq_lens (host, ulysses_degree*ring_degree entries) must sum per ring
+ *   group to that ring chunk's length, or be NULL for the default split.  head_counts (host,
+ *   ulysses_degree entries summing to H) or NULL for the default split of H.
+ *   1 <= ulysses_degree <= 16, 1 <= ring_degree <= 16, ulysses_degree <= H.
+ *   causal: key j visible to query i iff j <= i (global positions).
+ *   o: [B][S][H][D] of o_dt; lse: fp32 [B][S][H] or NULL.
+ *   workspace: device scratch of at least usp_attention_workspace_size(...) bytes, 256-byte
+ *   aligned; its first 4 bytes are the status word usp_check_status reads.
+ *   Steps (one stream): fused reorder + seq->head re-layout of Q, K, V; one partial-attention
+ *   launch over every (ring step, chunk pair, head, query tile) with fully masked causal tiles
+ *   skipped; LSE merge of the ring partials; fused head->seq re-layout + inverse reorder of O
+ *   and LSE.  Steps that are identities for the given grid are skipped.
+ *   Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA as above. */
+usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                           float scale, int causal, int ulysses_degree, int ring_degree,
+                           const int32_t* seq_lens, const int32_t* head_counts, usp_order_t order,
+                           void* o, usp_dtype_t o_dt, float* lse, void* workspace,
+                           size_t workspace_bytes, usp_stream_t stream);
+
+/* Bytes of workspace usp_attention needs for these arguments (0 on invalid arguments). */
+size_t usp_attention_workspace_size(int B, int S, int H, int D, int ulysses_degree,
+                                    int ring_degree, usp_order_t order, usp_dtype_t o_dt);
+
+/* Synchronises `stream`, reads the device status word at `status` (a usp_attention workspace or
+ * the uint32 given to usp_attn_partial), clears it, and returns USP_ERR_TIMEOUT if a bounded wait
+ * gave up since the last check, USP_ERR_CUDA if the stream reports an error, else USP_OK. */
+usp_status_t usp_check_status(void* status, usp_stream_t stream);
+
+/* Host-only planning query (no device needed): the chunk-pair work list usp_attention launches,
+ * for B = 1.  Writes up to `cap` records of 8 int32 each into `out`:
+ *   {ulysses index u, q ring chunk r, ring step k, kv ring chunk r2, q local row0, q rows,
+ *    visible kv rows, diag}
+ * where key c (0 <= c < visible kv rows, local to ring chunk r2) is visible to q local row i
+ * (row0 <= i < row0 + q rows) iff c <= i - row0 + diag (diag = INT32_MAX: no causal limit).
+ * Returns the total record count (which may exceed cap), or -1 on invalid arguments. */
+int usp_plan_pairs(int S, int ulysses_degree, int ring_degree, int causal, usp_order_t order,
+                   int32_t* out, int cap);
+
+const char* usp_status_string(usp_status_t s);
+const char* usp_last_error(void);
+int usp_version(void); /* major*10000 + minor*100 + patch */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* USP_GB300_H */
