@@ -161,11 +161,12 @@ usp_status_t usp_lse_merge(int n_parts, const float* o_parts, int64_t o_part_str
  *   the ordering fixes; seq_lens (host, ulysses_degree*ring_degree entries) must sum per ring
  *   group to that ring chunk's length, or be NULL for the default split.  head_counts (host,
  *   ulysses_degree entries summing to H) or NULL for the default split of H.
- *   1 <= ulysses_degree <= 16, 1 <= ring_degree <= 16, ulysses_degree <= H.
+ *   ulysses_degree >= 1, ring_degree >= 1, their product <= 16, ulysses_degree <= H.
  *   causal: key j visible to query i iff j <= i (global positions).
  *   o: [B][S][H][D] of o_dt; lse: fp32 [B][S][H] or NULL.
  *   workspace: device scratch of at least usp_attention_workspace_size(...) bytes, 256-byte
- *   aligned; its first 4 bytes are the status word usp_check_status reads.
+ *   aligned.  Its first 4 bytes are the status word usp_check_status reads and clears; zero
+ *   them once before the first call (e.g. allocate the workspace zeroed).
  *   Steps (one stream): fused reorder + seq->head re-layout of Q, K, V; one partial-attention
  *   launch over every (ring step, chunk pair, head, query tile) with fully masked causal tiles
  *   skipped; LSE merge of the ring partials; fused head->seq re-layout + inverse reorder of O

@@ -1,0 +1,487 @@
+// Partial attention on the 5th-generation tensor cores: for every (chunk pair, batch, head,
+// 128-row query tile) work unit, O = softmax(scale Q K^T + mask) V and its natural-log LSE
+// ([USP] the backend's (out, lse) for one ring step; [CP] Ring Attention).
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0      TMA producer: Q tile once per unit, then K and V tiles into a STAGES-deep ring.
+//   warp 1      MMA issuer (one thread) and TMEM owner:
+//                 S[j%2]  = Q K_j^T       (SS MMA, M=128, N=128, K=D, fp32 accumulate in TMEM)
+//                 O      += P_{j-1} V_{j-1} (TS MMA: P read from TMEM, V from shared memory)
+//               S of tile j is issued before P V of tile j-1, so the tensor core works on the
+//               next scores while the softmax warps exponentiate the current ones.
+//   warps 2-5   softmax warpgroup: thread = query row = TMEM lane.  Reads its S row with
+//               tcgen05.ld, masks, takes the row max, exponentiates with ex2, writes P (bf16)
+//               back to TMEM and keeps the row sum l in a register.  The running max is only
+//               raised when a tile's max exceeds it by more than 8 (in log2 units); then O is
+//               rescaled in TMEM.  Otherwise the stale max is kept, which bounds P by 2^8 and
+//               leaves the result exact after the final division by l.
+//               Epilogue: O / l to global memory (fp32 or bf16) and lse = (m + log2 l) ln 2.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O [384,384+D).
+//
+// Shared memory tiles are the canonical 128-byte-swizzled layouts TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B: rows of 64 bf16 (128 B), 8-row atoms of 1024 B.  Q and K are
+// K-major operands (head dim contiguous); V is the MN-major B operand of P V.
+//
+// Every mbarrier wait is bounded (see ptx.cuh); on a timeout all roles stop, drain their
+// in-flight copies and MMAs, free TMEM and exit, and the status word records the error.
+#include <algorithm>
+#include <cstring>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace usp {
+namespace {
+
+constexpr float kTau = 8.0f;  // lazy-rescale threshold, log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
+constexpr int kThreads = 192;
+
+template <int D, int STAGES>
+struct Layout {
+  static constexpr int kQBytes = kAttnBM * D * 2;
+  static constexpr int kKBytes = kAttnBN * D * 2;
+  static constexpr int kVBytes = kAttnBN * D * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kQBytes;
+  static constexpr int kV = kK + STAGES * kKBytes;
+  static constexpr int kBar = kV + STAGES * kVBytes;
+  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2],
+  // o_empty, mma_done
+  static constexpr int kNumBars = 2 + 3 * STAGES + 6 + 2;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kEnd = kAbort + 4;
+  static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
+};
+
+struct Unit {
+  const AttnSeg* seg;
+  int qt, b, h, q0, qv, n_kv;
+};
+
+__device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
+  int lo = 0, hi = p.n_segs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.segs[mid].unit0 <= unit) lo = mid; else hi = mid - 1;
+  }
+  const AttnSeg& s = p.segs[lo];
+  const int local = unit - s.unit0;
+  const int qi = local % s.n_qtiles;
+  const int hb = local / s.n_qtiles;
+  Unit u;
+  u.seg = &s;
+  u.qt = s.rev ? s.n_qtiles - 1 - qi : qi;
+  u.h = hb % s.n_heads;
+  u.b = hb / s.n_heads;
+  u.q0 = u.qt * kAttnBM;
+  u.qv = min(kAttnBM, s.q_len - u.q0);
+  int max_c = s.kv_len - 1;
+  if (s.diag != kNoDiag) max_c = min(max_c, u.q0 + u.qv - 1 + s.diag);
+  u.n_kv = max_c < 0 ? 0 : max_c / kAttnBN + 1;
+  return u;
+}
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+  using L = Layout<D, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* v_full = k_full + STAGES;
+  uint64_t* kv_empty = v_full + STAGES;
+  uint64_t* s_full = kv_empty + STAGES;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* o_empty = pv_done + 2;
+  uint64_t* mma_done = o_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t budget = p.budget_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(o_empty, 128);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, q_iter = 0;
+      uint32_t fills[STAGES];
+      for (int s = 0; s < STAGES; ++s) fills[s] = 0;
+      for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
+        const Unit u = decode_unit(p, unit);
+        if (u.n_kv == 0) continue;
+        const AttnSeg& s = *u.seg;
+        if (q_iter > 0 && !mbar_wait(q_empty, (q_iter - 1) & 1, abort_flag, p.status, budget)) break;
+        mbar_arrive_expect_tx(q_full, L::kQBytes);
+        const int qrow = s.q_row0 + u.b * s.q_bstride + u.q0;
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_3d(sm + L::kQ + blk * kAttnBM * 128, &p.maps[s.q_map], blk * 64, u.h, qrow, q_full);
+        ++q_iter;
+        const int kvrow = s.kv_row0 + u.b * s.kv_bstride;
+        bool ok = true;
+        for (int j = 0; j < u.n_kv; ++j) {
+          if (!mbar_wait(&kv_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
+          mbar_arrive_expect_tx(&k_full[stage], L::kKBytes);
+#pragma unroll
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_3d(sm + L::kK + stage * L::kKBytes + blk * kAttnBN * 128, &p.maps[s.k_map],
+                        blk * 64, u.h, kvrow + j * kAttnBN, &k_full[stage]);
+          mbar_arrive_expect_tx(&v_full[stage], L::kVBytes);
+#pragma unroll
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_3d(sm + L::kV + stage * L::kVBytes + blk * kAttnBN * 128, &p.maps[s.v_map],
+                        blk * 64, u.h, kvrow + j * kAttnBN, &v_full[stage]);
+          ++fills[stage];
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+      // drain: every issued copy has landed before the CTA may exit
+      for (int s = 0; s < STAGES; ++s) {
+        if (fills[s]) {
+          mbar_drain(&k_full[s], (fills[s] - 1) & 1, budget);
+          mbar_drain(&v_full[s], (fills[s] - 1) & 1, budget);
+        }
+      }
+      if (q_iter) mbar_drain(q_full, (q_iter - 1) & 1, budget);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kAttnBM, kAttnBN, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kAttnBM, D, 1);
+      const uint32_t q_base = smem_u32(sm + L::kQ);
+      const uint32_t k_base = smem_u32(sm + L::kK);
+      const uint32_t v_base = smem_u32(sm + L::kV);
+      uint32_t stage = 0, phase = 0, q_iter = 0, units_done = 0, g = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; unit < p.n_units && ok; unit += gridDim.x) {
+        const Unit u = decode_unit(p, unit);
+        if (u.n_kv == 0) continue;
+        if (!mbar_wait(q_full, q_iter & 1, abort_flag, p.status, budget)) break;
+        ++q_iter;
+        tc_fence_after();
+        uint32_t prev_stage = 0, prev_phase = 0;
+        for (int j = 0; j <= u.n_kv; ++j) {
+          if (j < u.n_kv) {
+            if (!mbar_wait(&k_full[stage], phase, abort_flag, p.status, budget)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sb = (g + j) & 1;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t qa = q_base + (kk >> 2) * (kAttnBM * 128) + (kk & 3) * 32;
+              const uint32_t ka = k_base + stage * L::kKBytes + (kk >> 2) * (kAttnBN * 128) + (kk & 3) * 32;
+              mma_ss(tmem + kColS + sb * 128, sdesc_sw128(qa, 16, 1024), sdesc_sw128(ka, 16, 1024),
+                     idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[sb]);
+            if (j == u.n_kv - 1) mma_commit(q_empty);
+          }
+          if (j > 0) {
+            const uint32_t gt = g + j - 1;
+            const uint32_t pb = gt & 1;
+            if (!mbar_wait(&p_full[pb], (gt >> 1) & 1, abort_flag, p.status, budget)) { ok = false; break; }
+            if (j == 1 && units_done > 0 &&
+                !mbar_wait(o_empty, (units_done - 1) & 1, abort_flag, p.status, budget)) { ok = false; break; }
+            if (!mbar_wait(&v_full[prev_stage], prev_phase, abort_flag, p.status, budget)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kAttnBN / 16; ++kk) {
+              const uint32_t va = v_base + prev_stage * L::kVBytes + kk * (16 * 128);
+              mma_ts(tmem + kColO, tmem + kColP + pb * 64 + kk * 8,
+                     sdesc_sw128(va, kAttnBN * 128, 1024), idesc_pv, (j > 1 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&pv_done[pb]);
+            mma_commit(&kv_empty[prev_stage]);
+          }
+          if (j < u.n_kv) {
+            prev_stage = stage;
+            prev_phase = phase;
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          }
+        }
+        g += u.n_kv;
+        ++units_done;
+      }
+      // drain: all issued MMAs complete before TMEM is freed
+      mma_commit(mma_done);
+      mbar_drain(mma_done, 0, budget);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroup
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
+    const float scale_log2 = p.scale_log2;
+    uint32_t g = 0;
+    bool ok = true;
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool r = mbar_wait(bar, parity, abort_flag, p.status, budget);
+      return __all_sync(0xffffffffu, r);
+    };
+    for (int unit = blockIdx.x; unit < p.n_units && ok; unit += gridDim.x) {
+      const Unit u = decode_unit(p, unit);
+      const AttnSeg& s = *u.seg;
+      const bool row_valid = row < u.qv;
+      const long long orow = static_cast<long long>(u.b) * s.o_bstride + s.o_row0 + u.q0 + row;
+      const long long o_elem = (orow * s.n_heads + u.h) * D;
+      if (u.n_kv == 0) {
+        if (row_valid) {
+          if (p.o_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.o) + o_elem);
+            for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(s.o) + o_elem);
+            for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          if (s.lse) s.lse[orow * s.n_heads + u.h] = -INFINITY;
+        }
+        continue;
+      }
+      const int qi = u.q0 + row;
+      const int lim = s.diag == kNoDiag ? INT_MAX : qi + s.diag;  // visible key c <= lim
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      for (int j = 0; j < u.n_kv; ++j, ++g) {
+        const uint32_t sb = g & 1;
+        if (!wait_all(&s_full[sb], (g >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        float x[kAttnBN];
+#pragma unroll
+        for (int c = 0; c < kAttnBN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_addr + kColS + sb * 128 + c * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]);
+        }
+        const int c0 = j * kAttnBN;
+        const bool need_mask = (c0 + kAttnBN > s.kv_len) ||
+                               (s.diag != kNoDiag && c0 + kAttnBN - 1 > u.q0 + s.diag);
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+        if (need_mask) {
+          const int last = min(s.kv_len - 1, lim) - c0;  // visible local columns: i <= last
+#pragma unroll
+          for (int i = 0; i < kAttnBN; ++i) {
+            x[i] = (i <= last) ? x[i] * scale_log2 : -INFINITY;
+            mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kAttnBN; ++i) {
+            x[i] *= scale_log2;
+            mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
+          }
+        }
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        float alpha = 1.f;
+        bool resc = false;
+        if (mx > m_ref + kTau) {
+          if (m_ref != -INFINITY) {
+            alpha = ex2_approx(m_ref - mx);
+            resc = true;
+          }
+          m_ref = mx;
+        }
+        const float base = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float sum8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
+        uint32_t pk[kAttnBN / 2];
+#pragma unroll
+        for (int i = 0; i < kAttnBN / 2; ++i) {
+          const float p0 = ex2_approx(x[2 * i] - base);
+          const float p1 = ex2_approx(x[2 * i + 1] - base);
+          sum8[i & 7] += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                         ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
+        // P[sb] was last read by P V of tile g-2
+        if (g >= 2 && !wait_all(&pv_done[sb], ((g >> 1) - 1) & 1)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < kAttnBN / 64; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = pk[c * 32 + i];
+          tmem_st32(tmem + lane_addr + kColP + sb * 64 + c * 32, r);
+        }
+        if (__any_sync(0xffffffffu, resc)) {
+          // O holds the sum through tile g-1: wait for that P V, then rescale in place
+          if (!wait_all(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_addr + kColO + c * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tmem + lane_addr + kColO + c * 32, r);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[sb]);
+      }
+      if (!ok) break;
+      // epilogue: wait for the unit's last P V
+      if (!wait_all(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      const float lse = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_addr + kColO + c * 32, r);
+        tmem_wait_ld();
+        if (row_valid) {
+          if (p.o_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.o) + o_elem + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              dst[i] = make_uint4(
+                  pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
+                  pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
+                  pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
+                  pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(s.o) + o_elem + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(r[4 * i + 0]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
+                                   __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(o_empty);
+      if (row_valid && s.lse) s.lse[orow * s.n_heads + u.h] = lse;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int STAGES>
+usp_status_t launch_one(const AttnParams& p, cudaStream_t stream) {
+  using L = Layout<D, STAGES>;
+  static_assert(L::kAlloc <= 232448, "shared memory budget");
+  auto kern = attn_fwd_kernel<D, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return fail(USP_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = std::max(1, std::min(p.n_units, sms));
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(p);
+  return check_launch("attention kernel");
+}
+
+}  // namespace
+
+usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D, int64_t rows,
+                          int64_t row_stride) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<EncodeFn>(fn);
+  }();
+  if (!encode) return fail(USP_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(n_heads),
+                              static_cast<cuuint64_t>(std::max<int64_t>(rows, 1))};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(row_stride) * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kAttnBM)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(USP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return USP_OK;
+}
+
+usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs, int D,
+                              cudaStream_t stream) {
+  // Longest units first: sort segments by the key tiles a full query tile visits.
+  auto cost = [](const AttnSeg& s) {
+    return s.diag == kNoDiag ? s.kv_len : std::min(s.kv_len, s.q_len + s.diag);
+  };
+  std::stable_sort(segs.begin(), segs.end(),
+                   [&](const AttnSeg& a, const AttnSeg& b) { return cost(a) > cost(b); });
+  size_t at = 0;
+  while (at < segs.size()) {
+    const size_t n = std::min<size_t>(kAttnMaxSegs, segs.size() - at);
+    int units = 0, used = 0;
+    for (size_t i = 0; i < n; ++i) {
+      AttnSeg s = segs[at + i];
+      s.n_qtiles = (s.q_len + kAttnBM - 1) / kAttnBM;
+      s.unit0 = units;
+      const long long add = static_cast<long long>(s.n_qtiles) * s.n_heads * p.B;
+      if (add == 0) continue;
+      if (units + add > INT_MAX / 2) return fail(USP_ERR_UNSUPPORTED, "too many attention work units");
+      units += static_cast<int>(add);
+      p.segs[used++] = s;
+    }
+    p.n_segs = used;
+    p.n_units = units;
+    if (units > 0) {
+      usp_status_t st = D == 64 ? launch_one<64, 4>(p, stream) : launch_one<128, 2>(p, stream);
+      if (st != USP_OK) return st;
+    }
+    at += n;
+  }
+  return USP_OK;
+}
+
+}  // namespace usp

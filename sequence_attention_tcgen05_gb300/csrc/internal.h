@@ -1,0 +1,140 @@
+// Host-side declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <vector>
+
+#include "usp.h"
+
+namespace usp {
+
+// ------------------------------------------------------------------------------------------
+// Errors: the thread-local message behind usp_last_error().
+// ------------------------------------------------------------------------------------------
+usp_status_t fail(usp_status_t s, const char* fmt, ...);
+usp_status_t check_launch(const char* what);
+usp_status_t check_device();  // current device must be sm_103
+
+inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Default split of n items over P parts: floor(n/P) + (p < n mod P).
+std::vector<int> default_split(int n, int P);
+
+// Global positions of ring rank r's local rows under an ordering (piecewise affine, <= 2 pieces).
+struct Positions {
+  int n_seg = 1;
+  int start[2] = {0, 0};
+  int len[2] = {0, 0};
+  int stride = 1;
+  int rows() const { return len[0] + (n_seg > 1 ? len[1] : 0); }
+  int64_t at(int i) const {
+    return i < len[0] ? int64_t(start[0]) + int64_t(i) * stride
+                      : int64_t(start[1]) + int64_t(i - len[0]) * stride;
+  }
+};
+std::vector<Positions> ring_positions(usp_order_t order, int S, int R);
+
+// ------------------------------------------------------------------------------------------
+// Re-layout (Ulysses all-to-all as a permutation, reorder, and their fusion).
+// Rows are enumerated as (ring group r, batch b, ring-local row l).  The "head side" is a set of
+// per-(r, head group g) buffers [B][S_r][h_g][D]; the "sequence side" is either packed chunks
+// (mode 0: chunk (r, u) = [B][len][H][D] holding ring-local rows [off, off + len)) or a global
+// [B][S][H][D] tensor addressed through the ordering's positions (mode 1).
+// ------------------------------------------------------------------------------------------
+constexpr int kRelayoutMaxR = 64;
+constexpr int kRelayoutMaxU = 64;
+constexpr int kRelayoutMaxRU = 256;
+
+struct RelayoutParams {
+  const char* src[3];
+  char* dst[3];
+  int n_tensors;
+  int B, H, D, elem;  // D = elements per head, elem = bytes per element
+  int R, U;
+  int seq_mode;  // 0 packed chunks, 1 global through positions
+  int dir;       // 0 sequence side -> head side, 1 head side -> sequence side
+  int S;         // global sequence length (mode 1)
+  long long row0[kRelayoutMaxR + 1];
+  int S_r[kRelayoutMaxR];
+  int h[kRelayoutMaxU];
+  int hoff[kRelayoutMaxU];
+  long long hbase[kRelayoutMaxRU];  // element offset of head-side block (r, g)
+  int c_off[kRelayoutMaxRU];        // mode 0: chunk (r, u)
+  int c_len[kRelayoutMaxRU];
+  long long c_base[kRelayoutMaxRU];
+  int p_start0[kRelayoutMaxR], p_len0[kRelayoutMaxR], p_start1[kRelayoutMaxR],
+      p_stride[kRelayoutMaxR];  // mode 1
+};
+
+usp_status_t launch_relayout(RelayoutParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// LSE merge.
+// ------------------------------------------------------------------------------------------
+usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_stride,
+                              const float* lse_parts, int64_t lse_part_stride, int64_t n_vec,
+                              int D, void* o_out, bool out_bf16, float* lse_out,
+                              cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// Partial attention (tcgen05).
+// ------------------------------------------------------------------------------------------
+constexpr int kAttnBM = 128;  // query rows per tile (one TMEM lane each)
+constexpr int kAttnBN = 128;  // key rows per tile
+constexpr int kAttnMaxMaps = 48;
+constexpr int kAttnMaxSegs = 128;
+constexpr int kNoDiag = INT_MAX;
+
+// One run of query rows against one key range: key c (0 <= c < kv_len) is visible to local
+// query row i (0 <= i < q_len) iff c <= i + diag (diag == kNoDiag: no limit).
+struct AttnSeg {
+  void* o;        // output block base (fp32 or bf16 per launch): rows [B][o_bstride], heads n_heads
+  float* lse;     // LSE block base (may be null)
+  int q_map, k_map, v_map;
+  int q_row0, q_bstride, q_len;
+  int kv_row0, kv_bstride, kv_len;
+  int diag;
+  int n_heads;
+  int o_row0, o_bstride;
+  int n_qtiles;
+  int unit0;
+  int rev;        // 1: visit query tiles last first (causal: longest first)
+  int pad;
+};
+
+struct AttnParams {
+  CUtensorMap maps[kAttnMaxMaps];
+  AttnSeg segs[kAttnMaxSegs];
+  int n_segs;
+  int n_units;
+  int B;
+  int o_bf16;
+  float scale_log2;
+  uint32_t* status;
+  unsigned long long budget_ns;
+};
+
+// A run of query rows produced by the chunk-pair planner.
+struct Run {
+  int q0, q_len, kv_len, diag;
+};
+// Runs for query rows with positions qp against key rows with positions kp (both increasing).
+// causal = false gives one run covering everything.
+std::vector<Run> plan_runs(const Positions& qp, const Positions& kp, bool causal);
+
+// Tensor map over a bf16 buffer of `rows` rows x `n_heads` heads x D, row stride in elements.
+usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D, int64_t rows,
+                          int64_t row_stride);
+
+// Launch over all segments (split into several launches if there are more than fit).
+usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs, int D,
+                              cudaStream_t stream);
+
+}  // namespace usp
+
+// Kernel parameters are passed by value; CUDA 12.1+ allows up to 32764 bytes of them.
+static_assert(sizeof(usp::AttnParams) <= 32764, "attention kernel parameters too large");
+static_assert(sizeof(usp::RelayoutParams) <= 32764, "relayout kernel parameters too large");

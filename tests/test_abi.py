@@ -1,0 +1,122 @@
+"""The C ABI on the CPU: the library builds and loads, exports every declared symbol, validates
+arguments without touching a GPU, and its chunk-pair planner agrees with the oracle's orderings."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from sequence_attention_tcgen05_gb300 import build, usp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INT32_MAX = 2**31 - 1
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build_library()
+    return usp.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "usp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(usp_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(usp.EXPORTED) == names
+
+
+def test_status_strings_and_version(L):
+    assert usp.usp_version() == 100
+    for s in range(7):
+        assert L.usp_status_string(s)
+
+
+def test_invalid_arguments_rejected_on_host(L):
+    lens = (ctypes.c_int32 * 2)(3, 4)
+    assert L.usp_relayout_seq2head(256, 512, 0, 1, 4, 8, 0, lens, None, None) == usp.USP_ERR_INVALID_ARG
+    neg = (ctypes.c_int32 * 2)(3, -1)
+    assert L.usp_relayout_seq2head(256, 512, 0, 1, 4, 8, 2, neg, None, None) == usp.USP_ERR_INVALID_ARG
+    bad_heads = (ctypes.c_int32 * 2)(1, 1)
+    assert L.usp_relayout_head2seq(256, 512, 0, 1, 4, 8, 2, lens, bad_heads, None) == usp.USP_ERR_INVALID_ARG
+    assert "head_counts" in L.usp_last_error().decode()
+    # D = 96 is valid but not built
+    assert L.usp_attn_partial(256, 256, 256, 1, 1, 8, 8, 96, 96, 96, 1.0, None, None, 256, 1,
+                              256, None, None) == usp.USP_ERR_UNSUPPORTED
+    # misaligned q
+    assert L.usp_attn_partial(258, 256, 256, 1, 1, 8, 8, 64, 64, 64, 1.0, None, None, 256, 1,
+                              256, None, None) == usp.USP_ERR_INVALID_ARG
+    # seq_lens not summing to the ring chunk
+    sl = (ctypes.c_int32 * 2)(5, 5)
+    assert L.usp_attention(256, 256, 256, 1, 11, 4, 64, 1.0, 0, 2, 1, sl, None, 0, 256, 1, 256,
+                           256, 1 << 30, None) == usp.USP_ERR_INVALID_ARG
+    # workspace too small
+    assert L.usp_attention(256, 256, 256, 1, 10, 4, 64, 1.0, 0, 2, 1, sl, None, 0, 256, 1, 256,
+                           256, 16, None) == usp.USP_ERR_WORKSPACE
+    assert L.usp_lse_merge(0, 256, 0, 256, 0, 1, 1, 4, 256, 1, 256, None) == usp.USP_ERR_INVALID_ARG
+    assert L.usp_lse_merge(17, 256, 0, 256, 0, 1, 1, 4, 256, 1, 256, None) == usp.USP_ERR_INVALID_ARG
+
+
+def test_workspace_size(L):
+    B, S, H, D = 1, 4608, 24, 128
+    n = usp.usp_attention_workspace_size(B, S, H, D, 2, 1)
+    # Q, K, V bf16 head-sharded copies + O (fp32) + LSE, + status
+    assert n >= 3 * S * H * D * 2 + S * H * D * 4 + S * H * 4
+    # pure contiguous ring on B = 1 needs no re-layout copies, only partials
+    r = usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3)
+    assert 3 * 1000 * 4 * 64 * 4 <= r < 3 * 1000 * 4 * 64 * 4 + 4 * 4096 + 3 * 1000 * 4 * 4 + 1024
+    assert usp.usp_attention_workspace_size(1, 10, 4, 96, 1, 1) == 0
+    assert usp.usp_attention_workspace_size(1, 10, 4, 64, 5, 4) == 0
+
+
+@pytest.mark.parametrize("S,U,R,causal,order", [
+    (1000, 1, 3, False, "contiguous"), (65536, 1, 8, True, "zigzag"), (61, 1, 5, True, "zigzag"),
+    (61, 1, 4, True, "stripe"), (7145, 2, 2, True, "contiguous"), (47, 2, 3, True, "stripe"),
+    (19, 1, 8, True, "contiguous"), (5, 1, 8, True, "zigzag"), (300, 3, 1, True, "contiguous"),
+])
+def test_planner_matches_oracle_visibility(L, S, U, R, causal, order):
+    """Every planned run reproduces, row by row, the number of visible keys the oracle's global
+    positions give, and the runs of each (u, r, step) tile the ring chunk exactly."""
+    pos = oracle.ring_positions(order, S, R)
+    recs = usp.usp_plan_pairs(S, U, R, causal, order)
+    cover = {}
+    for (u, r, k, r2, q0, qlen, kvlen, diag) in recs:
+        assert r2 == (r - k) % R
+        qp = pos[r][q0:q0 + qlen]
+        vis = (pos[r2][None, :] <= qp[:, None]).sum(axis=1) if causal else np.full(qlen, len(pos[r2]))
+        i = np.arange(qlen)
+        if diag == INT32_MAX:
+            want = np.full(qlen, kvlen)
+        else:
+            want = np.clip(i + diag + 1, 0, kvlen)
+        assert np.array_equal(vis, want), (u, r, k, q0)
+        cover.setdefault((u, r, k), []).append((q0, qlen))
+    assert len(cover) == U * R * sum(1 for p in pos if len(p) > 0)
+    for (u, r, k), runs in cover.items():
+        runs.sort()
+        at = 0
+        for q0, qlen in runs:
+            assert q0 == at
+            at += qlen
+        assert at == len(pos[r])
+
+
+def test_planner_counts_every_causal_pair_once(L):
+    """Across all ring steps, the planned runs see each causal (query, key) pair exactly once:
+    sum over runs of the visible-key counts is S(S+1)/2, the count the FLOP figure uses."""
+    for S, U, R, order in [(65536, 1, 8, "zigzag"), (7145, 2, 2, "contiguous"), (999, 1, 4, "stripe")]:
+        total = 0
+        for (u, r, k, r2, q0, qlen, kvlen, d) in usp.usp_plan_pairs(S, U, R, True, order):
+            i = np.arange(qlen, dtype=np.int64)
+            vis = np.full(qlen, kvlen) if d == INT32_MAX else np.clip(i + d + 1, 0, kvlen)
+            if u == 0:
+                total += int(vis.sum())
+        assert total == S * (S + 1) // 2
