@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Benchmark of usp_attention, the whole context-parallel attention path, on synthetic inputs.
+
+One step = one usp_attention call on the workload (fused reorder + seq->head re-layout of Q, K, V;
+the partial-attention launch over every chunk pair; the LSE merge of ring partials; the fused
+head->seq re-layout of O and LSE).  Inputs are resident in HBM when the timed region starts; the
+L2 cache is flushed between steps (outside the step's events) because the inputs of the default
+workload fit in L2.  Times come from CUDA events on the launching stream.
+
+  value     attention TFLOP/s of the whole step: algorithmic FLOPs 4 B H D x (visible query/key
+            pairs) over the step's device time (all phases), summed over ranks.
+  e2e       the same metric through the C ABI with the inputs in pinned host memory: each step
+            copies Q, K, V host->device, runs usp_attention and copies O and LSE back.
+  roofline  the partial-attention phase alone against the measured dense bf16 tensor peak.
+
+Multi-GPU: the method is partitioned onto virtual ranks of one GPU, so N GPUs run N independent
+replicas (weak scaling); the only cross-rank traffic is the timing reduction.
+
+``--impl reference`` times the fp64 CPU oracle (the reference arm: a deliberately slow program)
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s & % bf16 tensor peak; re-layout+merge GB/s & % HBM BW"
+DEFAULT_WORKLOAD = "flux_1024_u2"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_HBM_GBS = 8000.0
+
+# DRAM bytes (read + write) per launch of the partial-attention kernel from an ncu capture, with
+# the hash of the kernel sources they were taken on; reported as null once the kernel changes.
+ATTN_TRAFFIC = {}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attn.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "sequence_attention_tcgen05_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ------------------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max over ranks of a host scalar (identity on one process)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index] if device is not None else None)
+        else:
+            dist.barrier()
+
+
+def aggregate(units_per_rank: float, seconds_this_rank: float, world: int, device=None):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    t = reduce_max(seconds_this_rank, device)
+    return world * units_per_rank / t, t
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="usp_clocks_", suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+        self.marks = []
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except Exception:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, 1e30)
+        inside = [r for r in rows if t0 - 1 <= r[0] <= t1 + 1]
+        window = "timed region"
+        if len(inside) < 3:
+            inside, window = rows, "warm-up and timed region"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------------------------------------
+# workload helpers
+# ------------------------------------------------------------------------------------------------
+
+def workload(name: str):
+    from sequence_attention_tcgen05_gb300 import synth
+    return synth.WORKLOADS[name]
+
+
+def phase_bytes(w, out_elem: int):
+    """Algorithmic HBM bytes of the bandwidth-bound phases (each element read once + written once)."""
+    elems = w.B * w.S * w.H * w.D
+    rows_h = w.B * w.S * w.H
+    relayout = not (w.ulysses_degree == 1 and (w.ring_degree == 1 or (w.order == "contiguous" and w.B == 1)))
+    b = {"qkv_relayout": 2 * 3 * elems * 2 if relayout else 0}
+    if w.ring_degree > 1:
+        b["merge"] = w.ring_degree * (elems * 4 + rows_h * 4) + elems * out_elem + rows_h * 4
+    else:
+        b["merge"] = 0
+    b["out_relayout"] = 2 * (elems * out_elem + rows_h * 4) if relayout else 0
+    return b
+
+
+def cpu_oracle_sample(w, target_s: float, rng_seed: int = 0):
+    """Time the fp64 oracle on query rows of one head: returns (TFLOP/s, seconds, description)."""
+    import numpy as np
+
+    import oracle
+    from sequence_attention_tcgen05_gb300 import synth
+    h = 0
+    kb = synth.qkv_rows_bits(w.seed, synth.STREAM_K, w.B, w.S, w.H, w.D, 0, np.arange(w.S), h,
+                             w.text_rows, w.text_scale)
+    vb = synth.qkv_rows_bits(w.seed, synth.STREAM_V, w.B, w.S, w.H, w.D, 0, np.arange(w.S), h,
+                             w.text_rows, w.text_scale)
+    k, v = oracle.widen_bf16(kb), oracle.widen_bf16(vb)
+    scale = 1.0 / math.sqrt(w.D)
+
+    def run(rows):
+        qb = synth.qkv_rows_bits(w.seed, synth.STREAM_Q, w.B, w.S, w.H, w.D, 0, rows, h,
+                                 w.text_rows, w.text_scale)
+        q = oracle.widen_bf16(qb)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, scale, w.causal, rows)
+        dt = time.perf_counter() - t0
+        vis = (rows + 1).sum() if w.causal else len(rows) * w.S
+        return 4.0 * w.D * vis, dt
+
+    n = 64
+    rng = np.random.default_rng(rng_seed)
+    fl, dt = run(np.sort(rng.choice(w.S, n, replace=False)))
+    n = int(min(w.S, max(64, n * target_s / max(dt, 1e-3))))
+    rows = np.sort(rng.choice(w.S, n, replace=False))
+    fl, dt = run(rows)
+    return fl / dt / 1e12, dt, f"{n} query rows of head 0 (of {w.S} rows x {w.H} heads), full key set"
+
+
+def cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------------------------------------
+# arms
+# ------------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = workload(args.workload)
+    # each step a bounded sample, sized so the whole run stays within about two minutes
+    per_step = max(0.5, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    vals, secs = [], []
+    for i in range(args.warmup + args.steps):
+        v, dt, desc = cpu_oracle_sample(w, per_step, rng_seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+            secs.append(dt)
+    value = sum(v * s for v, s in zip(vals, secs)) / sum(secs)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * statistics.mean(secs), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, "fp64"),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, out_dtype: str):
+    return {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D,
+            "ulysses_degree": w.ulysses_degree, "ring_degree": w.ring_degree,
+            "causal": w.causal, "order": w.order, "text_rows": w.text_rows,
+            "seq_lens": list(w.seq_lens) or "default split", "out_dtype": out_dtype,
+            "l2": "flushed between timed steps (256 MiB write outside the step events)"}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from sequence_attention_tcgen05_gb300 import build, synth, usp
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    build.build_library()
+    usp.lib()
+    w = workload(args.workload)
+    out_dt = torch.bfloat16 if args.out_dtype == "bf16" else torch.float32
+    o_code = usp.USP_BF16 if out_dt == torch.bfloat16 else usp.USP_FP32
+    out_elem = 2 if out_dt == torch.bfloat16 else 4
+    B, S, H, D = w.B, w.S, w.H, w.D
+    scale = 1.0 / math.sqrt(D)
+    flops = w.attention_flops()
+
+    qb, kb, vb = synth.make_qkv_bits(B, S, H, D, w.seed, w.text_rows, w.text_scale)
+    host = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (qb, kb, vb)]
+    q, k, v = (x.to(device) for x in host)
+    o = torch.empty((B, S, H, D), dtype=out_dt, device=device)
+    lse = torch.empty((B, S, H), dtype=torch.float32, device=device)
+    nbytes = usp.usp_attention_workspace_size(B, S, H, D, w.ulysses_degree, w.ring_degree,
+                                              w.order, o_code)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)  # 256 MiB > L2
+    stream = torch.cuda.current_stream()
+    seq = list(w.seq_lens) or None
+
+    def make_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        for e in evs:
+            e.record(stream)  # materialise the handle
+        return evs
+
+    events = make_events()
+    handles = [e.cuda_event for e in events]
+
+    def step():
+        return usp.usp_attention_events(q, k, v, B, S, H, D, scale, w.causal, w.ulysses_degree,
+                                        w.ring_degree, o, lse, ws, nbytes, handles, seq, None,
+                                        w.order, o_code, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if usp.usp_check_status(ws) != usp.USP_OK:
+        raise RuntimeError("device status after warm-up: " + usp.lib().usp_last_error().decode())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    phases = {"qkv_relayout": 0.0, "attention": 0.0, "merge": 0.0, "out_relayout": 0.0}
+    total_ms = 0.0
+    launches = 0
+    barrier(device)
+    torch.cuda.synchronize()
+    clocks.mark()
+    for _ in range(args.steps):
+        flush.zero_()
+        launches += step()
+        events[4].synchronize()
+        t = [events[i].elapsed_time(events[i + 1]) for i in range(4)]
+        phases["qkv_relayout"] += t[0]
+        phases["attention"] += t[1]
+        phases["merge"] += t[2]
+        phases["out_relayout"] += t[3]
+        total_ms += sum(t)
+    torch.cuda.synchronize()
+    barrier(device)
+    clocks.mark()
+    clk = clocks.stop()
+    status = usp.usp_check_status(ws)
+    if status != usp.USP_OK:
+        raise RuntimeError("device status after timing: " + usp.lib().usp_last_error().decode())
+    value, t_max = aggregate(args.steps * flops, total_ms / 1000.0, world, device)
+    value /= 1e12
+
+    # end to end through the C ABI with host buffers
+    e2e_steps = max(3, min(args.steps, 50))
+    o_host = torch.empty(o.shape, dtype=out_dt).pin_memory()
+    l_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for i in range(e2e_steps + 1):
+        flush.zero_()
+        e_start.record(stream)
+        for dst, src in zip((q, k, v), host):
+            dst.copy_(src, non_blocking=True)
+        usp.usp_attention(q, k, v, B, S, H, D, scale, w.causal, w.ulysses_degree, w.ring_degree,
+                          o, lse, ws, nbytes, seq, None, w.order, o_code, stream)
+        o_host.copy_(o, non_blocking=True)
+        l_host.copy_(lse, non_blocking=True)
+        e_end.record(stream)
+        e_end.synchronize()
+        if i > 0:
+            e2e_ms += e_start.elapsed_time(e_end)
+    e2e_value, _ = aggregate(e2e_steps * flops, e2e_ms / 1000.0, world, device)
+    h2d = 3 * B * S * H * D * 2
+    d2h = B * S * H * D * out_elem + B * S * H * 4
+
+    peaks, peak_kind = load_peaks()
+    att_s = phases["attention"] / 1000.0 / args.steps
+    achieved = flops / att_s / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = ATTN_TRAFFIC.get(w.name)
+    traffic_bytes = traffic["bytes"] if traffic and traffic["kernel_hash"] == kernel_hash() else None
+    pb = phase_bytes(w, out_elem)
+    bw = {}
+    for name in ("qkv_relayout", "merge", "out_relayout"):
+        if pb[name]:
+            s = phases[name] / 1000.0 / args.steps
+            gbs = pb[name] / s / 1e9
+            bw[name] = {"GB/s": gbs, "bytes": pb[name], "us": s * 1e6,
+                        "frac_measured_hbm": gbs / peaks["hbm_gbs"], "frac_8TBs": gbs / NOMINAL_HBM_GBS}
+    bw_bytes = sum(pb.values())
+    bw_s = sum(phases[n] for n in ("qkv_relayout", "merge", "out_relayout")) / 1000.0 / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_max * 1000.0 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, args.out_dtype),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic_bytes,
+                     "kernel": "attn_fwd_kernel (partial attention, all chunk pairs, one launch)",
+                     "peak_kind": f"{peak_kind} bf16 burst",
+                     "frac_sustained_peak": achieved / peaks["bf16_tflops_sustained"]},
+        "relayout_merge": {"GB/s": bw_bytes / bw_s / 1e9 if bw_s > 0 else None,
+                           "frac_measured_hbm": (bw_bytes / bw_s / 1e9 / peaks["hbm_gbs"]) if bw_s > 0 else None,
+                           "frac_8TBs": (bw_bytes / bw_s / 1e9 / NOMINAL_HBM_GBS) if bw_s > 0 else None,
+                           "phases": bw},
+        "phases_ms_per_step": {k: v / args.steps for k, v in phases.items()},
+        "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cv, cdt, desc = cpu_oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": cv, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
+                                "sample": desc, "seconds": cdt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--out-dtype", choices=["bf16", "fp32"], default="bf16")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

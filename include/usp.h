@@ -178,6 +178,21 @@ usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, i
                            void* o, usp_dtype_t o_dt, float* lse, void* workspace,
                            size_t workspace_bytes, usp_stream_t stream);
 
+/* usp_attention with phase timing: identical work, and additionally records the caller's CUDA
+ * events (cudaEvent_t handles, created by the caller) on `stream`:
+ *   events[0] before the first launch, events[1] after the Q/K/V re-layout, events[2] after the
+ *   partial-attention launch(es), events[3] after the merge, events[4] after the output
+ *   re-layout.  A skipped phase records its event at the same point as the previous one.
+ *   `events` must hold 5 handles (entries may be NULL to skip a record).  If `n_launches` is not
+ *   NULL it receives the number of kernels launched.  Errors as usp_attention. */
+usp_status_t usp_attention_events(const void* q, const void* k, const void* v, int B, int S, int H,
+                                  int D, float scale, int causal, int ulysses_degree,
+                                  int ring_degree, const int32_t* seq_lens,
+                                  const int32_t* head_counts, usp_order_t order, void* o,
+                                  usp_dtype_t o_dt, float* lse, void* workspace,
+                                  size_t workspace_bytes, void* const* events, int* n_launches,
+                                  usp_stream_t stream);
+
 /* Bytes of workspace usp_attention needs for these arguments (0 on invalid arguments). */
 size_t usp_attention_workspace_size(int B, int S, int H, int D, int ulysses_degree,
                                     int ring_degree, usp_order_t order, usp_dtype_t o_dt);

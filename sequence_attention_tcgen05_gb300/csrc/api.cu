@@ -482,12 +482,22 @@ size_t usp_attention_workspace_size(int B, int S, int H, int D, int ulysses_degr
   return g.total;
 }
 
-usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
-                           float scale, int causal, int ulysses_degree, int ring_degree,
-                           const int32_t* seq_lens, const int32_t* head_counts, usp_order_t order,
-                           void* o, usp_dtype_t o_dt, float* lse, void* workspace,
-                           size_t workspace_bytes, usp_stream_t stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+static usp_status_t attention_impl(const void* q, const void* k, const void* v, int B, int S, int H,
+                                   int D, float scale, int causal, int ulysses_degree,
+                                   int ring_degree, const int32_t* seq_lens,
+                                   const int32_t* head_counts, usp_order_t order, void* o,
+                                   usp_dtype_t o_dt, float* lse, void* workspace,
+                                   size_t workspace_bytes, void* const* events, int* n_launches,
+                                   cudaStream_t stream) {
+  int launches = 0;
+  auto mark = [&](int i) -> usp_status_t {
+    if (events && events[i]) {
+      cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream);
+      if (e != cudaSuccess) return fail(USP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
+    }
+    return USP_OK;
+  };
+  if (n_launches) *n_launches = 0;
   if (!q || !k || !v || !o) return fail(USP_ERR_INVALID_ARG, "NULL q, k, v or o");
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)))
     return fail(USP_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
@@ -500,6 +510,7 @@ usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, i
     return fail(USP_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, g.total);
   if (S == 0) return USP_OK;
   if (usp_status_t st = check_device()) return st;
+  if (usp_status_t st = mark(0)) return st;
   char* ws = static_cast<char*>(workspace);
   const int U = g.U, R = g.R;
   const int oel = o_dt == USP_BF16 ? 2 : 4;
@@ -518,8 +529,10 @@ usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, i
     rp.src[2] = static_cast<const char*>(v); rp.dst[2] = ws + g.off_v;
     rp.dir = 0;
     if ((st = launch_relayout(rp, stream))) return st;
+    ++launches;
     wq = ws + g.off_q; wk = ws + g.off_k; wv = ws + g.off_v;
   }
+  if ((st = mark(1))) return st;
 
   // 2. partial attention over every (Ulysses rank, q ring chunk, ring step) pair in one launch
   static thread_local AttnParams params;
@@ -580,6 +593,8 @@ usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, i
     }
   }
   if ((st = launch_attention(p, segs, D, stream))) return st;
+  launches += static_cast<int>((segs.size() + kAttnMaxSegs - 1) / kAttnMaxSegs);
+  if ((st = mark(2))) return st;
 
   // 3. merge the ring partials
   char* fin_o = g.relayout ? ws + g.off_wo : static_cast<char*>(o);
@@ -589,7 +604,9 @@ usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, i
                                reinterpret_cast<const float*>(ws + g.off_lpart), int64_t(B) * S * H,
                                int64_t(B) * S * H, D, fin_o, o_dt == USP_BF16, fin_l, stream)))
       return st;
+    ++launches;
   }
+  if ((st = mark(3))) return st;
 
   // 4. fused head -> seq re-layout + inverse reorder of O and LSE
   if (g.relayout) {
@@ -600,6 +617,7 @@ usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, i
     rp.dst[0] = static_cast<char*>(o);
     rp.dir = 1;
     if ((st = launch_relayout(rp, stream))) return st;
+    ++launches;
     if (lse) {
       fill_relayout_grid(rp, g, 1, 4);
       rp.n_tensors = 1;
@@ -607,9 +625,34 @@ usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, i
       rp.dst[0] = reinterpret_cast<char*>(lse);
       rp.dir = 1;
       if ((st = launch_relayout(rp, stream))) return st;
+      ++launches;
     }
   }
+  if ((st = mark(4))) return st;
+  if (n_launches) *n_launches = launches;
   return USP_OK;
+}
+
+usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                           float scale, int causal, int ulysses_degree, int ring_degree,
+                           const int32_t* seq_lens, const int32_t* head_counts, usp_order_t order,
+                           void* o, usp_dtype_t o_dt, float* lse, void* workspace,
+                           size_t workspace_bytes, usp_stream_t stream) {
+  return attention_impl(q, k, v, B, S, H, D, scale, causal, ulysses_degree, ring_degree, seq_lens,
+                        head_counts, order, o, o_dt, lse, workspace, workspace_bytes, nullptr,
+                        nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+usp_status_t usp_attention_events(const void* q, const void* k, const void* v, int B, int S, int H,
+                                  int D, float scale, int causal, int ulysses_degree,
+                                  int ring_degree, const int32_t* seq_lens,
+                                  const int32_t* head_counts, usp_order_t order, void* o,
+                                  usp_dtype_t o_dt, float* lse, void* workspace,
+                                  size_t workspace_bytes, void* const* events, int* n_launches,
+                                  usp_stream_t stream) {
+  return attention_impl(q, k, v, B, S, H, D, scale, causal, ulysses_degree, ring_degree, seq_lens,
+                        head_counts, order, o, o_dt, lse, workspace, workspace_bytes, events,
+                        n_launches, reinterpret_cast<cudaStream_t>(stream));
 }
 
 usp_status_t usp_check_status(void* status, usp_stream_t stream) {

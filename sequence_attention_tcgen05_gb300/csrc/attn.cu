@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t budget = p.budget_ns;
+  const uint64_t drain_budget = budget < 200000000ull ? budget : 200000000ull;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -170,11 +171,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // drain: every issued copy has landed before the CTA may exit
       for (int s = 0; s < STAGES; ++s) {
         if (fills[s]) {
-          mbar_drain(&k_full[s], (fills[s] - 1) & 1, budget);
-          mbar_drain(&v_full[s], (fills[s] - 1) & 1, budget);
+          mbar_drain(&k_full[s], (fills[s] - 1) & 1, drain_budget);
+          mbar_drain(&v_full[s], (fills[s] - 1) & 1, drain_budget);
         }
       }
-      if (q_iter) mbar_drain(q_full, (q_iter - 1) & 1, budget);
+      if (q_iter) mbar_drain(q_full, (q_iter - 1) & 1, drain_budget);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       // drain: all issued MMAs complete before TMEM is freed
       mma_commit(mma_done);
-      mbar_drain(mma_done, 0, budget);
+      mbar_drain(mma_done, 0, drain_budget);
     }
   } else {
     // ------------------------------------------------------------------ softmax warpgroup

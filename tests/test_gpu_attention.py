@@ -1,0 +1,102 @@
+"""usp_attn_partial (tcgen05 kernel) against the fp64 oracle on the same seeded bf16 inputs."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from sequence_attention_tcgen05_gb300 import synth, usp
+
+from gpu_util import Guarded, check_attention, to_dev_bf16, torch, widen
+
+pytestmark = pytest.mark.gpu
+
+
+def run_partial(B, H, Sq, Sk, D, q_pos=None, k_pos=None, seed=0, out="fp32", packed=False):
+    t = torch()
+    qb = synth.make_tensor_bits(seed, 0, B, Sq, H, D)
+    kb = synth.make_tensor_bits(seed, 1, B, Sk, H, D)
+    vb = synth.make_tensor_bits(seed, 2, B, Sk, H, D)
+    if packed:
+        # q, k, v rows interleaved as [B][S][3][H][D] (QKV-packed layout): row stride 3*H*D
+        assert Sq == Sk
+        pk = np.stack([qb, kb, vb], axis=2)
+        dev = to_dev_bf16(pk.reshape(-1))
+        n3 = H * D
+        q, k, v = dev[0:], dev[n3:], dev[2 * n3:]
+        qs = ks = 3 * H * D
+    else:
+        q, k, v = to_dev_bf16(qb), to_dev_bf16(kb), to_dev_bf16(vb)
+        qs = ks = H * D
+    dt = t.float32 if out == "fp32" else t.bfloat16
+    o = Guarded((B, Sq, H, D), dt)
+    lse = Guarded((B, Sq, H), t.float32)
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    qp = usp.Positions.make(*q_pos) if q_pos else None
+    kp = usp.Positions.make(*k_pos) if k_pos else None
+    usp.usp_attn_partial(q, k, v, B, H, Sq, Sk, D, qs, ks, scale, o.view, lse.view, qp, kp,
+                         status=status)
+    assert usp.usp_check_status(status) == usp.USP_OK
+    o.check()
+    lse.check()
+    return (o.view.float().cpu().numpy(), lse.view.cpu().numpy(),
+            widen(qb), widen(kb), widen(vb), scale)
+
+
+def positions(spec):
+    segs, stride = spec
+    return np.concatenate([s + stride * np.arange(n) for s, n in segs]).astype(np.int64)
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,D", [
+    (1, 1, 128, 128, 128), (1, 1, 128, 128, 64), (1, 2, 200, 333, 64), (2, 3, 257, 129, 128),
+    (1, 1, 1, 1, 64), (1, 2, 5, 700, 128), (1, 4, 1000, 1000, 64), (1, 2, 384, 2500, 128)])
+def test_noncausal(B, H, Sq, Sk, D):
+    o, l, q, k, v, scale = run_partial(B, H, Sq, Sk, D)
+    ro, rl = oracle.attention(q, k, v, scale)
+    check_attention(o, l, ro, rl, f"noncausal {B},{H},{Sq},{Sk},{D}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("qspec,kspec", [
+    (([(0, 300)], 1), ([(0, 300)], 1)),                       # diagonal chunk
+    (([(500, 260)], 1), ([(0, 700)], 1)),                     # later q chunk, mixed tiles
+    (([(0, 130)], 1), ([(200, 150)], 1)),                     # q entirely before k: all masked
+    (([(0, 100), (700, 100)], 1), ([(0, 100), (700, 100)], 1)),   # zigzag, own rank
+    (([(0, 100), (700, 100)], 1), ([(100, 100), (600, 100)], 1)),  # zigzag, other rank
+    (([(1, 150)], 4), ([(3, 150)], 4)),                       # stripe, r < r2
+    (([(3, 150)], 4), ([(1, 150)], 4)),                       # stripe, r > r2
+])
+def test_causal_positions(D, qspec, kspec):
+    Sq = sum(n for _, n in qspec[0])
+    Sk = sum(n for _, n in kspec[0])
+    o, l, q, k, v, scale = run_partial(1, 2, Sq, Sk, D, qspec, kspec, seed=5)
+    ro, rl = oracle.attention(q, k, v, scale, True, positions(qspec), positions(kspec))
+    check_attention(o, l, ro, rl, f"causal {qspec} {kspec}")
+
+
+def test_empty_kv_chunk():
+    t = torch()
+    B, H, Sq, D = 1, 2, 150, 64
+    qb = synth.make_tensor_bits(0, 0, B, Sq, H, D)
+    q = to_dev_bf16(qb)
+    kv = to_dev_bf16(qb[:, :1])
+    o = Guarded((B, Sq, H, D), t.float32)
+    lse = Guarded((B, Sq, H), t.float32)
+    usp.usp_attn_partial(q, kv, kv, B, H, Sq, 0, D, H * D, H * D, 0.125, o.view, lse.view)
+    t.cuda.synchronize()
+    o.check()
+    assert bool((o.view == 0).all()) and bool(t.isneginf(lse.view).all())
+
+
+def test_bf16_output_and_packed_qkv():
+    o, l, q, k, v, scale = run_partial(2, 3, 300, 300, 128, out="bf16", packed=True)
+    ro, rl = oracle.attention(q, k, v, scale)
+    check_attention(o, l, ro, rl, "bf16 packed")
+
+
+def test_repeat_calls_identical():
+    a = run_partial(1, 4, 640, 900, 128, seed=9)
+    b = run_partial(1, 4, 640, 900, 128, seed=9)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
