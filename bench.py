@@ -43,7 +43,10 @@ NOMINAL_HBM_GBS = 8000.0
 
 # DRAM bytes (read + write) per launch of the partial-attention kernel from an ncu capture, with
 # the hash of the kernel sources they were taken on; reported as null once the kernel changes.
-ATTN_TRAFFIC = {}
+ATTN_TRAFFIC = {
+    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.066240 MB + write 6.801664 MB
+    "flux_1024_u2": {"bytes": 91867904, "kernel_hash": "a85fe08c6694de74"},
+}
 
 
 def kernel_hash() -> str:
@@ -197,36 +200,32 @@ def phase_bytes(w, out_elem: int):
 
 
 def cpu_oracle_sample(w, target_s: float, rng_seed: int = 0):
-    """Time the fp64 oracle on query rows of one head: returns (TFLOP/s, seconds, description)."""
+    """Time the fp64 oracle on whole heads of the workload (all query rows of a head against its
+    full key set) until about ``target_s`` seconds have passed or every head is done; returns
+    (TFLOP/s, seconds, description of the sample)."""
     import numpy as np
 
     import oracle
     from sequence_attention_tcgen05_gb300 import synth
-    h = 0
-    kb = synth.qkv_rows_bits(w.seed, synth.STREAM_K, w.B, w.S, w.H, w.D, 0, np.arange(w.S), h,
-                             w.text_rows, w.text_scale)
-    vb = synth.qkv_rows_bits(w.seed, synth.STREAM_V, w.B, w.S, w.H, w.D, 0, np.arange(w.S), h,
-                             w.text_rows, w.text_scale)
-    k, v = oracle.widen_bf16(kb), oracle.widen_bf16(vb)
     scale = 1.0 / math.sqrt(w.D)
-
-    def run(rows):
-        qb = synth.qkv_rows_bits(w.seed, synth.STREAM_Q, w.B, w.S, w.H, w.D, 0, rows, h,
-                                 w.text_rows, w.text_scale)
-        q = oracle.widen_bf16(qb)
+    rows = np.arange(w.S)
+    vis = (rows + 1).sum() if w.causal else w.S * w.S
+    heads = list(np.random.default_rng(rng_seed).permutation(w.H))
+    done_flops, spent, n = 0.0, 0.0, 0
+    for h in heads:
+        bits = [synth.qkv_rows_bits(w.seed, st, w.B, w.S, w.H, w.D, 0, rows, int(h), w.text_rows,
+                                    w.text_scale) for st in (synth.STREAM_Q, synth.STREAM_K,
+                                                             synth.STREAM_V)]
+        q, k, v = (oracle.widen_bf16(b) for b in bits)
         t0 = time.perf_counter()
         oracle.attention_rows(q, k, v, scale, w.causal, rows)
-        dt = time.perf_counter() - t0
-        vis = (rows + 1).sum() if w.causal else len(rows) * w.S
-        return 4.0 * w.D * vis, dt
-
-    n = 64
-    rng = np.random.default_rng(rng_seed)
-    fl, dt = run(np.sort(rng.choice(w.S, n, replace=False)))
-    n = int(min(w.S, max(64, n * target_s / max(dt, 1e-3))))
-    rows = np.sort(rng.choice(w.S, n, replace=False))
-    fl, dt = run(rows)
-    return fl / dt / 1e12, dt, f"{n} query rows of head 0 (of {w.S} rows x {w.H} heads), full key set"
+        spent += time.perf_counter() - t0
+        done_flops += 4.0 * w.D * vis
+        n += 1
+        if spent >= target_s:
+            break
+    return (done_flops / spent / 1e12, spent,
+            f"{n} of {w.H} heads (batch 0), every query row against the full key set")
 
 
 def cores() -> int:
@@ -246,7 +245,7 @@ def run_reference(args):
         return 0
     w = workload(args.workload)
     # each step a bounded sample, sized so the whole run stays within about two minutes
-    per_step = max(0.5, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    per_step = max(0.2, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     vals, secs = [], []
     for i in range(args.warmup + args.steps):
         v, dt, desc = cpu_oracle_sample(w, per_step, rng_seed=i)
