@@ -193,6 +193,31 @@ usp_status_t usp_attention_events(const void* q, const void* k, const void* v, i
                                   size_t workspace_bytes, void* const* events, int* n_launches,
                                   usp_stream_t stream);
 
+/* usp_attention_noalloc — usp_attention without a workspace, for callers that cannot allocate
+ * device memory: code embedded in a host application that owns every device allocation, or
+ * latency-critical paths where cudaMalloc's implicit synchronisation is not acceptable.  The pages
+ * have no counterpart to this entry point; it is a library convenience.
+ *
+ *   Same arguments and results as usp_attention, minus the workspace.  The scratch is a 128 MiB
+ *   array compiled into the library (a file-scope __device__ array): every GPU that loads the
+ *   library's device code holds it until the process exits.  Problems whose
+ *   usp_attention_workspace_size exceeds 128 MiB are rejected with USP_ERR_WORKSPACE and a message
+ *   giving both sizes; nothing is launched then.
+ *   The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *   with that device current) and caches it; make that first call before any stream capture.
+ *   Every call shares the array and finds the previous call's data in it; each call clears the
+ *   status word it needs zeroed.  Calls that overlap on the GPU (several streams or host threads
+ *   on one device) race on the array: serialise them.
+ *   status: optional device uint32 that receives this call's bounded-wait status word (pass it to
+ *   usp_check_status), or NULL.
+ *   This entry point calls no cudaMalloc or cudaFree and no allocating library routine. */
+usp_status_t usp_attention_noalloc(const void* q, const void* k, const void* v, int B, int S, int H,
+                                   int D, float scale, int causal, int ulysses_degree,
+                                   int ring_degree, const int32_t* seq_lens,
+                                   const int32_t* head_counts, usp_order_t order, void* o,
+                                   usp_dtype_t o_dt, float* lse, uint32_t* status,
+                                   usp_stream_t stream);
+
 /* Bytes of workspace usp_attention needs for these arguments (0 on invalid arguments). */
 size_t usp_attention_workspace_size(int B, int S, int H, int D, int ulysses_degree,
                                     int ring_degree, usp_order_t order, usp_dtype_t o_dt);

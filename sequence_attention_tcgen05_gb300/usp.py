@@ -19,7 +19,8 @@ ORDERS = {"contiguous": 0, "zigzag": 1, "stripe": 2}
 
 EXPORTED = [
     "usp_relayout_seq2head", "usp_relayout_head2seq", "usp_reorder", "usp_attn_partial",
-    "usp_lse_merge", "usp_attention", "usp_attention_events", "usp_attention_workspace_size",
+    "usp_lse_merge", "usp_attention", "usp_attention_events", "usp_attention_noalloc",
+    "usp_attention_workspace_size",
     "usp_check_status",
     "usp_plan_pairs", "usp_status_string", "usp_last_error", "usp_version",
 ]
@@ -74,6 +75,8 @@ def lib() -> ctypes.CDLL:
         "usp_attention_events": [vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, i32p, i32p,
                                  i32, vp, i32, vp, vp, sz, ctypes.POINTER(vp),
                                  ctypes.POINTER(ctypes.c_int), vp],
+        "usp_attention_noalloc": [vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, i32p, i32p,
+                                  i32, vp, i32, vp, vp, vp],
         "usp_attention_workspace_size": [i32, i32, i32, i32, i32, i32, i32, i32],
         "usp_check_status": [vp, vp],
         "usp_plan_pairs": [i32, i32, i32, i32, i32, i32p, i32],
@@ -203,6 +206,17 @@ def usp_attention_events(q, k, v, B, S, H, D, scale, causal, ulysses_degree, rin
                                       _ptr(workspace), workspace_bytes, ev, ctypes.byref(n),
                                       _stream(stream)), "usp_attention_events")
     return n.value
+
+
+def usp_attention_noalloc(q, k, v, B, S, H, D, scale, causal, ulysses_degree, ring_degree, o, lse,
+                          seq_lens=None, head_counts=None, order="contiguous", o_dt=None,
+                          status=None, stream=None):
+    """usp_attention on the library's built-in scratch (no workspace argument, no allocation)."""
+    o_dt = _dtype(o) if o_dt is None else o_dt
+    _check(lib().usp_attention_noalloc(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, float(scale),
+                                       int(causal), ulysses_degree, ring_degree, _i32(seq_lens),
+                                       _i32(head_counts), ORDERS[order], _ptr(o), o_dt, _ptr(lse),
+                                       _ptr(status), _stream(stream)), "usp_attention_noalloc")
 
 
 def usp_check_status(status, stream=None) -> int:
