@@ -1,22 +1,27 @@
 // Partial attention on the 5th-generation tensor cores: for every (chunk pair, batch, head,
-// 128-row query tile) work unit, O = softmax(scale Q K^T + mask) V and its natural-log LSE
+// 256-row query block) work unit, O = softmax(scale Q K^T + mask) V and its natural-log LSE
 // ([USP] the backend's (out, lse) for one ring step; [CP] Ring Attention).
 //
-// One persistent CTA per SM, 6 warps:
-//   warp 0      TMA producer: Q tile once per unit, then K and V tiles into a STAGES-deep ring.
-//   warp 1      MMA issuer (one thread) and TMEM owner:
-//                 S[j%2]  = Q K_j^T       (SS MMA, M=128, N=128, K=D, fp32 accumulate in TMEM)
-//                 O      += P_{j-1} V_{j-1} (TS MMA: P read from TMEM, V from shared memory)
-//               S of tile j is issued before P V of tile j-1, so the tensor core works on the
-//               next scores while the softmax warps exponentiate the current ones.
-//   warps 2-5   softmax warpgroup: thread = query row = TMEM lane.  Reads its S row with
-//               tcgen05.ld, masks, takes the row max, exponentiates with ex2, writes P (bf16)
-//               back to TMEM and keeps the row sum l in a register.  The running max is only
-//               raised when a tile's max exceeds it by more than 8 (in log2 units); then O is
-//               rescaled in TMEM.  Otherwise the stale max is kept, which bounds P by 2^8 and
-//               leaves the result exact after the final division by l.
-//               Epilogue: O / l to global memory (fp32 or bf16) and lse = (m + log2 l) ln 2.
-// TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O [384,384+D).
+// One persistent CTA per SM, three warpgroups (384 threads):
+//   WG0  warp 0: TMA producer — the unit's two 128-row Q tiles, then K and V tiles into a
+//                STAGES-deep ring (K and V of a key tile serve both query tiles).
+//        warp 1: MMA issuer (one thread) and TMEM owner.  Per key tile j, in this order:
+//                  S_a = Q_a K_j^T,  O_b += P_b(j-1) V_{j-1},  S_b = Q_b K_j^T,  O_a += P_a(j) V_j
+//                (SS MMA M=128 N=128 for the scores; TS MMA with P read from TMEM for P V), so the
+//                softmax of each query tile overlaps a score MMA and a P V MMA of the other tile.
+//        warps 2-3 idle.  The warpgroup gives registers away (setmaxnreg) to the softmax groups.
+//   WG1, WG2  softmax of query tile a / b: thread = query row = TMEM lane.  One 128-column
+//                tcgen05.ld of the S row, masking on boundary tiles, row max, exp2 of
+//                (s - max) * scale log2e with packed fp32x2 fused multiply-adds, bf16 P written
+//                back over the first 64 columns of S, row sum in registers.  The running max is
+//                raised only when a tile's max exceeds it by more than 8 (log2 units); then O is
+//                rescaled in TMEM.  Otherwise the stale max stays, which bounds P by 2^8 and is
+//                exact after the final division by the row sum.  Epilogue: O / l to global memory
+//                (fp32 or bf16) and lse = (m + log2 l) ln 2.
+// TMEM (512 columns): S_a [0,128) S_b [128,256) O_a [256,256+D) O_b [256+D,256+2D); P_x aliases
+// the first 64 columns of S_x.  MMAs issued by one thread execute in issue order, so a completed
+// S_x(j) implies P V of tile j-1 of the same query tile has completed: S_x may then be read, P_x
+// rewritten and O_x rescaled without another wait.
 //
 // Shared memory tiles are the canonical 128-byte-swizzled layouts TMA writes with
 // CU_TENSOR_MAP_SWIZZLE_128B: rows of 64 bf16 (128 B), 8-row atoms of 1024 B.  Q and K are
@@ -35,21 +40,24 @@ namespace {
 
 constexpr float kTau = 8.0f;  // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+// Register split: 384 threads x 168 at launch = 64512 >= 128 x 80 (WG0) + 256 x 208 (softmax).
+constexpr uint32_t kRegsWG0 = 80;
+constexpr uint32_t kRegsSoftmax = 208;
+static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 
 template <int D, int STAGES>
 struct Layout {
-  static constexpr int kQBytes = kAttnBM * D * 2;
+  static constexpr int kQTile = kAttnBM * D * 2;  // one 128-row Q tile
   static constexpr int kKBytes = kAttnBN * D * 2;
   static constexpr int kVBytes = kAttnBN * D * 2;
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQBytes;
+  static constexpr int kK = kQ + 2 * kQTile;
   static constexpr int kV = kK + STAGES * kKBytes;
   static constexpr int kBar = kV + STAGES * kVBytes;
   // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2],
-  // o_empty, mma_done
-  static constexpr int kNumBars = 2 + 3 * STAGES + 6 + 2;
+  // o_empty[2], mma_done
+  static constexpr int kNumBars = 2 + 3 * STAGES + 9;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
@@ -58,7 +66,8 @@ struct Layout {
 
 struct Unit {
   const AttnSeg* seg;
-  int qt, b, h, q0, qv, n_kv;
+  int b, h, q0, n_kv;
+  int qv[2];  // valid rows of tiles a and b
 };
 
 __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
@@ -69,17 +78,19 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
   }
   const AttnSeg& s = p.segs[lo];
   const int local = unit - s.unit0;
-  const int qi = local % s.n_qtiles;
-  const int hb = local / s.n_qtiles;
+  const int qi = local % s.n_qblk;
+  const int hb = local / s.n_qblk;
   Unit u;
   u.seg = &s;
-  u.qt = s.rev ? s.n_qtiles - 1 - qi : qi;
+  const int qb = s.rev ? s.n_qblk - 1 - qi : qi;
   u.h = hb % s.n_heads;
   u.b = hb / s.n_heads;
-  u.q0 = u.qt * kAttnBM;
-  u.qv = min(kAttnBM, s.q_len - u.q0);
+  u.q0 = qb * kAttnUnitRows;
+  u.qv[0] = max(0, min(kAttnBM, s.q_len - u.q0));
+  u.qv[1] = max(0, min(kAttnBM, s.q_len - u.q0 - kAttnBM));
+  const int last_row = u.q0 + u.qv[0] + u.qv[1] - 1;
   int max_c = s.kv_len - 1;
-  if (s.diag != kNoDiag) max_c = min(max_c, u.q0 + u.qv - 1 + s.diag);
+  if (s.diag != kNoDiag) max_c = min(max_c, last_row + s.diag);
   u.n_kv = max_c < 0 ? 0 : max_c / kAttnBN + 1;
   return u;
 }
@@ -96,15 +107,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* k_full = bars + 2;
   uint64_t* v_full = k_full + STAGES;
   uint64_t* kv_empty = v_full + STAGES;
-  uint64_t* s_full = kv_empty + STAGES;
+  uint64_t* s_full = kv_empty + STAGES;  // [2]: query tile a, b
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_empty = pv_done + 2;
-  uint64_t* mma_done = o_empty + 1;
+  uint64_t* mma_done = o_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbort);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int wg = warp >> 2;
   const uint64_t budget = p.budget_ns;
   const uint64_t drain_budget = budget < 200000000ull ? budget : 200000000ull;
 
@@ -120,8 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
+      mbar_init(&o_empty[i], 128);
     }
-    mbar_init(o_empty, 128);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -132,9 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  if (wg == 0) {
+    regs_dec<kRegsWG0>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
       uint32_t stage = 0, phase = 0, q_iter = 0;
       uint32_t fills[STAGES];
       for (int s = 0; s < STAGES; ++s) fills[s] = 0;
@@ -143,11 +156,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (u.n_kv == 0) continue;
         const AttnSeg& s = *u.seg;
         if (q_iter > 0 && !mbar_wait(q_empty, (q_iter - 1) & 1, abort_flag, p.status, budget)) break;
-        mbar_arrive_expect_tx(q_full, L::kQBytes);
+        mbar_arrive_expect_tx(q_full, 2 * L::kQTile);
         const int qrow = s.q_row0 + u.b * s.q_bstride + u.q0;
 #pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_3d(sm + L::kQ + blk * kAttnBM * 128, &p.maps[s.q_map], blk * 64, u.h, qrow, q_full);
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_3d(sm + L::kQ + x * L::kQTile + blk * kAttnBM * 128, &p.maps[s.q_map], blk * 64,
+                        u.h, qrow + x * kAttnBM, q_full);
         ++q_iter;
         const int kvrow = s.kv_row0 + u.b * s.kv_bstride;
         bool ok = true;
@@ -168,7 +184,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         if (!ok) break;
       }
-      // drain: every issued copy has landed before the CTA may exit
       for (int s = 0; s < STAGES; ++s) {
         if (fills[s]) {
           mbar_drain(&k_full[s], (fills[s] - 1) & 1, drain_budget);
@@ -176,17 +191,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       }
       if (q_iter) mbar_drain(q_full, (q_iter - 1) & 1, drain_budget);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kAttnBM, kAttnBN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kAttnBM, D, 1);
       const uint32_t q_base = smem_u32(sm + L::kQ);
       const uint32_t k_base = smem_u32(sm + L::kK);
       const uint32_t v_base = smem_u32(sm + L::kV);
-      uint32_t stage = 0, phase = 0, q_iter = 0, units_done = 0, g = 0;
+      uint32_t stage = 0, phase = 0, q_iter = 0, units_done = 0;
+      uint32_t gp[2] = {0, 0};  // P V count per query tile
       bool ok = true;
+      auto qk = [&](int x, uint32_t st) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qa = q_base + x * L::kQTile + (kk >> 2) * (kAttnBM * 128) + (kk & 3) * 32;
+          const uint32_t ka = k_base + st * L::kKBytes + (kk >> 2) * (kAttnBN * 128) + (kk & 3) * 32;
+          mma_ss(tmem + x * 128, sdesc_sw128(qa, 16, 1024), sdesc_sw128(ka, 16, 1024), idesc_qk,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[x]);
+      };
+      // O_x += P_x V(st); `first` = first key tile of the unit (overwrites O_x)
+      auto pv = [&](int x, uint32_t st, uint32_t ph, bool first) -> bool {
+        if (!mbar_wait(&p_full[x], gp[x] & 1, abort_flag, p.status, budget)) return false;
+        if (first && units_done > 0 &&
+            !mbar_wait(&o_empty[x], (units_done - 1) & 1, abort_flag, p.status, budget))
+          return false;
+        if (!mbar_wait(&v_full[st], ph, abort_flag, p.status, budget)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kAttnBN / 16; ++kk) {
+          const uint32_t va = v_base + st * L::kVBytes + kk * (16 * 128);
+          mma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8, sdesc_sw128(va, kAttnBN * 128, 1024),
+                 idesc_pv, (!first || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&pv_done[x]);
+        ++gp[x];
+        return true;
+      };
       for (int unit = blockIdx.x; unit < p.n_units && ok; unit += gridDim.x) {
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
@@ -194,45 +236,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ++q_iter;
         tc_fence_after();
         uint32_t prev_stage = 0, prev_phase = 0;
-        for (int j = 0; j <= u.n_kv; ++j) {
-          if (j < u.n_kv) {
-            if (!mbar_wait(&k_full[stage], phase, abort_flag, p.status, budget)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t sb = (g + j) & 1;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t qa = q_base + (kk >> 2) * (kAttnBM * 128) + (kk & 3) * 32;
-              const uint32_t ka = k_base + stage * L::kKBytes + (kk >> 2) * (kAttnBN * 128) + (kk & 3) * 32;
-              mma_ss(tmem + kColS + sb * 128, sdesc_sw128(qa, 16, 1024), sdesc_sw128(ka, 16, 1024),
-                     idesc_qk, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&s_full[sb]);
-            if (j == u.n_kv - 1) mma_commit(q_empty);
-          }
+        for (int j = 0; j < u.n_kv; ++j) {
+          if (!mbar_wait(&k_full[stage], phase, abort_flag, p.status, budget)) { ok = false; break; }
+          tc_fence_after();
+          qk(0, stage);
           if (j > 0) {
-            const uint32_t gt = g + j - 1;
-            const uint32_t pb = gt & 1;
-            if (!mbar_wait(&p_full[pb], (gt >> 1) & 1, abort_flag, p.status, budget)) { ok = false; break; }
-            if (j == 1 && units_done > 0 &&
-                !mbar_wait(o_empty, (units_done - 1) & 1, abort_flag, p.status, budget)) { ok = false; break; }
-            if (!mbar_wait(&v_full[prev_stage], prev_phase, abort_flag, p.status, budget)) { ok = false; break; }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kAttnBN / 16; ++kk) {
-              const uint32_t va = v_base + prev_stage * L::kVBytes + kk * (16 * 128);
-              mma_ts(tmem + kColO, tmem + kColP + pb * 64 + kk * 8,
-                     sdesc_sw128(va, kAttnBN * 128, 1024), idesc_pv, (j > 1 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&pv_done[pb]);
+            if (!pv(1, prev_stage, prev_phase, j == 1)) { ok = false; break; }
             mma_commit(&kv_empty[prev_stage]);
           }
-          if (j < u.n_kv) {
-            prev_stage = stage;
-            prev_phase = phase;
-            if (++stage == STAGES) { stage = 0; phase ^= 1; }
-          }
+          qk(1, stage);
+          if (j == u.n_kv - 1) mma_commit(q_empty);
+          if (!pv(0, stage, phase, j == 0)) { ok = false; break; }
+          prev_stage = stage;
+          prev_phase = phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
-        g += u.n_kv;
+        if (!ok) break;
+        if (!pv(1, prev_stage, prev_phase, u.n_kv == 1)) { ok = false; break; }
+        mma_commit(&kv_empty[prev_stage]);
         ++units_done;
       }
       // drain: all issued MMAs complete before TMEM is freed
@@ -240,11 +261,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_drain(mma_done, 0, drain_budget);
     }
   } else {
-    // ------------------------------------------------------------------ softmax warpgroup
+    // ------------------------------------------------------------------ softmax warpgroups
+    regs_inc<kRegsSoftmax>();
+    const int x = wg - 1;  // query tile a (0) or b (1)
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
-    const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
-    const float scale_log2 = p.scale_log2;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t t_s = t_lane + x * 128;
+    const uint32_t t_o = t_lane + 256 + x * D;
+    const float c = p.scale_log2;  // > 0 (checked on the host)
+    const uint64_t c2 = f2_pack(c, c);
     uint32_t g = 0;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -254,8 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     for (int unit = blockIdx.x; unit < p.n_units && ok; unit += gridDim.x) {
       const Unit u = decode_unit(p, unit);
       const AttnSeg& s = *u.seg;
-      const bool row_valid = row < u.qv;
-      const long long orow = static_cast<long long>(u.b) * s.o_bstride + s.o_row0 + u.q0 + row;
+      const int q0 = u.q0 + x * kAttnBM;  // first local row of this query tile
+      const bool row_valid = row < u.qv[x];
+      const long long orow = static_cast<long long>(u.b) * s.o_bstride + s.o_row0 + q0 + row;
       const long long o_elem = (orow * s.n_heads + u.h) * D;
       if (u.n_kv == 0) {
         if (row_valid) {
@@ -270,45 +297,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         continue;
       }
-      const int qi = u.q0 + row;
-      const int lim = s.diag == kNoDiag ? INT_MAX : qi + s.diag;  // visible key c <= lim
-      float m_ref = -INFINITY;
+      const int lim = s.diag == kNoDiag ? INT_MAX : q0 + row + s.diag;  // visible key c <= lim
+      float m_ref = -INFINITY;  // running max of scale*log2e*s, raised lazily
       float l = 0.f;
       for (int j = 0; j < u.n_kv; ++j, ++g) {
-        const uint32_t sb = g & 1;
-        if (!wait_all(&s_full[sb], (g >> 1) & 1)) { ok = false; break; }
+        if (!wait_all(&s_full[x], g & 1)) { ok = false; break; }
         tc_fence_after();
-        float x[kAttnBN];
-#pragma unroll
-        for (int c = 0; c < kAttnBN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_addr + kColS + sb * 128 + c * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]);
-        }
+        uint32_t r[kAttnBN];
+        tmem_ld128(t_s, r);
+        tmem_wait_ld();
         const int c0 = j * kAttnBN;
         const bool need_mask = (c0 + kAttnBN > s.kv_len) ||
-                               (s.diag != kNoDiag && c0 + kAttnBN - 1 > u.q0 + s.diag);
-        float mx8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+                               (s.diag != kNoDiag && c0 + kAttnBN - 1 > q0 + s.diag);
         if (need_mask) {
           const int last = min(s.kv_len - 1, lim) - c0;  // visible local columns: i <= last
 #pragma unroll
-          for (int i = 0; i < kAttnBN; ++i) {
-            x[i] = (i <= last) ? x[i] * scale_log2 : -INFINITY;
-            mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < kAttnBN; ++i) {
-            x[i] *= scale_log2;
-            mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
-          }
+          for (int i = 0; i < kAttnBN; ++i)
+            if (i > last) r[i] = 0xff800000u;  // -inf
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        float m8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(r[i]);
+#pragma unroll
+        for (int i = 8; i < kAttnBN; i += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            m8[k] = fmax3(m8[k], __uint_as_float(r[i + 2 * k]), __uint_as_float(r[i + 2 * k + 1]));
+        const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                               fmaxf(m8[6], m8[7])) * c;
         float alpha = 1.f;
         bool resc = false;
         if (mx > m_ref + kTau) {
@@ -318,81 +334,87 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
           m_ref = mx;
         }
-        const float base = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float sum8[8];
+        const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        const uint64_t nb2 = f2_pack(nb, nb);
+        uint64_t sum2[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
-        uint32_t pk[kAttnBN / 2];
+        for (int i = 0; i < 4; ++i) sum2[i] = 0ull;
 #pragma unroll
-        for (int i = 0; i < kAttnBN / 2; ++i) {
-          const float p0 = ex2_approx(x[2 * i] - base);
-          const float p1 = ex2_approx(x[2 * i + 1] - base);
-          sum8[i & 7] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int col = half * 64 + 2 * i;
+            const uint64_t a2 =
+                f2_fma(f2_pack(__uint_as_float(r[col]), __uint_as_float(r[col + 1])), c2, nb2);
+            float e0, e1;
+            f2_unpack(a2, e0, e1);
+            const float p0 = ex2_approx(e0);
+            const float p1 = ex2_approx(e1);
+            sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(t_s + half * 32, pk);
         }
-        l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                         ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
-        // P[sb] was last read by P V of tile g-2
-        if (g >= 2 && !wait_all(&pv_done[sb], ((g >> 1) - 1) & 1)) { ok = false; break; }
-#pragma unroll
-        for (int c = 0; c < kAttnBN / 64; ++c) {
-          uint32_t r[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = pk[c * 32 + i];
-          tmem_st32(tmem + lane_addr + kColP + sb * 64 + c * 32, r);
-        }
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        f2_unpack(sum2[0], s0, s1);
+        f2_unpack(sum2[1], s2, s3);
+        f2_unpack(sum2[2], s4, s5);
+        f2_unpack(sum2[3], s6, s7);
+        l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
         if (__any_sync(0xffffffffu, resc)) {
-          // O holds the sum through tile g-1: wait for that P V, then rescale in place
-          if (!wait_all(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
+          // S_x(j) complete => P V of tile j-1 complete: O_x is stable
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_addr + kColO + c * 32, r);
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t w[32];
+            tmem_ld32(t_o + cc * 32, w);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tmem + lane_addr + kColO + c * 32, r);
+            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+            tmem_st32(t_o + cc * 32, w);
           }
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full[sb]);
+        mbar_arrive(&p_full[x]);
       }
       if (!ok) break;
-      // epilogue: wait for the unit's last P V
-      if (!wait_all(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) { ok = false; break; }
+      // epilogue: wait for the unit's last P V of this tile
+      if (!wait_all(&pv_done[x], (g - 1) & 1)) { ok = false; break; }
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const float lse = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + kColO + c * 32, r);
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t o[64];
+        tmem_ld64(t_o + half * 64, o);
         tmem_wait_ld();
+        if (half == D / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(&o_empty[x]);
+        }
         if (row_valid) {
           if (p.o_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.o) + o_elem + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              dst[i] = make_uint4(
-                  pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
-                  pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
-                  pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
-                  pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(s.o) + o_elem + c * 32);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.o) + o_elem + half * 64);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(r[4 * i + 0]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
-                                   __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+              dst[i] = make_uint4(
+                  pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(s.o) + o_elem + half * 64);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              dst[i] = make_float4(__uint_as_float(o[4 * i + 0]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                   __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(o_empty);
-      if (row_valid && s.lse) s.lse[orow * s.n_heads + u.h] = lse;
+      if (row_valid) {
+        if (s.lse) s.lse[orow * s.n_heads + u.h] = lse;
+      }
     }
   }
 
@@ -454,7 +476,8 @@ usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D
 
 usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs, int D,
                               cudaStream_t stream) {
-  // Longest units first: sort segments by the key tiles a full query tile visits.
+  if (!(p.scale_log2 > 0.f)) return fail(USP_ERR_INVALID_ARG, "the softmax scale must be positive");
+  // Longest units first: sort segments by the keys a full query block visits.
   auto cost = [](const AttnSeg& s) {
     return s.diag == kNoDiag ? s.kv_len : std::min(s.kv_len, s.q_len + s.diag);
   };
@@ -466,9 +489,9 @@ usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs, int D,
     int units = 0, used = 0;
     for (size_t i = 0; i < n; ++i) {
       AttnSeg s = segs[at + i];
-      s.n_qtiles = (s.q_len + kAttnBM - 1) / kAttnBM;
+      s.n_qblk = (s.q_len + kAttnUnitRows - 1) / kAttnUnitRows;
       s.unit0 = units;
-      const long long add = static_cast<long long>(s.n_qtiles) * s.n_heads * p.B;
+      const long long add = static_cast<long long>(s.n_qblk) * s.n_heads * p.B;
       if (add == 0) continue;
       if (units + add > INT_MAX / 2) return fail(USP_ERR_UNSUPPORTED, "too many attention work units");
       units += static_cast<int>(add);

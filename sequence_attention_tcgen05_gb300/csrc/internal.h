@@ -84,6 +84,7 @@ usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_
 // ------------------------------------------------------------------------------------------
 constexpr int kAttnBM = 128;  // query rows per tile (one TMEM lane each)
 constexpr int kAttnBN = 128;  // key rows per tile
+constexpr int kAttnUnitRows = 2 * kAttnBM;  // query rows per work unit (two tiles per CTA)
 constexpr int kAttnMaxMaps = 48;
 constexpr int kAttnMaxSegs = 128;
 constexpr int kNoDiag = INT_MAX;
@@ -99,9 +100,9 @@ struct AttnSeg {
   int diag;
   int n_heads;
   int o_row0, o_bstride;
-  int n_qtiles;
+  int n_qblk;     // 256-row query blocks (work units per batch and head)
   int unit0;
-  int rev;        // 1: visit query tiles last first (causal: longest first)
+  int rev;        // 1: visit query blocks last first (causal: longest first)
   int pad;
 };
 
