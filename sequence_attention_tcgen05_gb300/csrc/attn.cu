@@ -11,13 +11,15 @@
 //                softmax of each query tile overlaps a score MMA and a P V MMA of the other tile.
 //        warps 2-3 idle.  The warpgroup gives registers away (setmaxnreg) to the softmax groups.
 //   WG1, WG2  softmax of query tile a / b: thread = query row = TMEM lane.  One 128-column
-//                tcgen05.ld of the S row, masking on boundary tiles, row max, exp2 of
-//                (s - max) * scale log2e with packed fp32x2 fused multiply-adds, bf16 P written
-//                back over the first 64 columns of S, row sum in registers.  The running max is
-//                raised only when a tile's max exceeds it by more than 8 (log2 units); then O is
-//                rescaled in TMEM.  Otherwise the stale max stays, which bounds P by 2^8 and is
-//                exact after the final division by the row sum.  Epilogue: O / l to global memory
-//                (fp32 or bf16) and lse = (m + log2 l) ln 2.
+//                tcgen05.ld of the S row, masking on boundary tiles, exp2 of
+//                s * scale log2e - m with packed fp32x2 fused multiply-adds, bf16 P written back
+//                over the first 64 columns of S, row sum in registers.  The running max m is raised
+//                only when a tile's max exceeds it by more than 8 (log2 units), and then O is
+//                rescaled in TMEM; otherwise the stale max stays, which bounds P by 2^8 and is
+//                exact after the final division by the row sum.  So once a row has a reference max
+//                the exponentials are computed against it straight away while the tile max is taken
+//                in the same pass (the exponentials are redone only when the max is raised).
+//                Epilogue: O / l to global memory (fp32 or bf16) and lse = (m + log2 l) ln 2.
 // TMEM (512 columns): S_a [0,128) S_b [128,256) O_a [256,256+D) O_b [256+D,256+2D); P_x aliases
 // the first 64 columns of S_x.  MMAs issued by one thread execute in issue order, so a completed
 // S_x(j) implies P V of tile j-1 of the same query tile has completed: S_x may then be read, P_x
@@ -93,6 +95,61 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
   if (s.diag != kNoDiag) max_c = min(max_c, last_row + s.diag);
   u.n_kv = max_c < 0 ? 0 : max_c / kAttnBN + 1;
   return u;
+}
+
+__device__ __forceinline__ float row_max(const uint32_t (&r)[kAttnBN]) {
+  float m8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(r[i]);
+#pragma unroll
+  for (int i = 8; i < kAttnBN; i += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      m8[k] = fmax3(m8[k], __uint_as_float(r[i + 2 * k]), __uint_as_float(r[i + 2 * k + 1]));
+  return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+}
+
+// One pass over a 128-column score row: p = 2^(s * c + nb) for every column (MUFU ex2), written
+// as bf16 P over the first 64 TMEM columns at t_p; returns the fp32 row sum.  MAX: also returns
+// the raw row max in *mraw.
+template <bool MAX>
+__device__ __forceinline__ float exp_pass(const uint32_t (&r)[kAttnBN], uint64_t c2, float nb,
+                                          uint32_t t_p, float* mraw) {
+  const uint64_t nb2 = f2_pack(nb, nb);
+  uint64_t sum2[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sum2[i] = 0ull;
+  float m8[8];
+  if (MAX) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+  }
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int col = half * 64 + 2 * i;
+      const float s0 = __uint_as_float(r[col]), s1 = __uint_as_float(r[col + 1]);
+      if (MAX) m8[i & 7] = fmax3(m8[i & 7], s0, s1);
+      const uint64_t a2 = f2_fma(f2_pack(s0, s1), c2, nb2);
+      float e0, e1;
+      f2_unpack(a2, e0, e1);
+      const float p0 = ex2_approx(e0);
+      const float p1 = ex2_approx(e1);
+      sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
+      pk[i] = pack_bf16x2(p0, p1);
+    }
+    tmem_st32(t_p + half * 32, pk);
+  }
+  if (MAX)
+    *mraw = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+  float s0, s1, s2, s3, s4, s5, s6, s7;
+  f2_unpack(sum2[0], s0, s1);
+  f2_unpack(sum2[1], s2, s3);
+  f2_unpack(sum2[2], s4, s5);
+  f2_unpack(sum2[3], s6, s7);
+  return ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
 }
 
 template <int D, int STAGES>
@@ -315,53 +372,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           for (int i = 0; i < kAttnBN; ++i)
             if (i > last) r[i] = 0xff800000u;  // -inf
         }
-        float m8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(r[i]);
-#pragma unroll
-        for (int i = 8; i < kAttnBN; i += 16)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            m8[k] = fmax3(m8[k], __uint_as_float(r[i + 2 * k]), __uint_as_float(r[i + 2 * k + 1]));
-        const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
-                               fmaxf(m8[6], m8[7])) * c;
         float alpha = 1.f;
         bool resc = false;
-        if (mx > m_ref + kTau) {
-          if (m_ref != -INFINITY) {
-            alpha = ex2_approx(m_ref - mx);
-            resc = true;
+        float sum;
+        if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+          // no reference max yet in this warp: take the tile max first
+          const float mx = row_max(r) * c;
+          if (mx > m_ref + kTau) {
+            if (m_ref != -INFINITY) {
+              alpha = ex2_approx(m_ref - mx);
+              resc = true;
+            }
+            m_ref = mx;
           }
-          m_ref = mx;
-        }
-        const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref;
-        const uint64_t nb2 = f2_pack(nb, nb);
-        uint64_t sum2[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sum2[i] = 0ull;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int col = half * 64 + 2 * i;
-            const uint64_t a2 =
-                f2_fma(f2_pack(__uint_as_float(r[col]), __uint_as_float(r[col + 1])), c2, nb2);
-            float e0, e1;
-            f2_unpack(a2, e0, e1);
-            const float p0 = ex2_approx(e0);
-            const float p1 = ex2_approx(e1);
-            sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
-            pk[i] = pack_bf16x2(p0, p1);
+          const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref;
+          sum = exp_pass<false>(r, c2, nb, t_s, nullptr);
+        } else {
+          // speculate: exponentiate against the running max while taking the tile max
+          float mraw;
+          sum = exp_pass<true>(r, c2, -m_ref, t_s, &mraw);
+          const float mx = mraw * c;
+          const bool raise = mx > m_ref + kTau;
+          if (__any_sync(0xffffffffu, raise)) {
+            if (raise) {
+              alpha = ex2_approx(m_ref - mx);
+              resc = true;
+              m_ref = mx;
+            }
+            sum = exp_pass<false>(r, c2, -m_ref, t_s, nullptr);
           }
-          tmem_st32(t_s + half * 32, pk);
         }
-        float s0, s1, s2, s3, s4, s5, s6, s7;
-        f2_unpack(sum2[0], s0, s1);
-        f2_unpack(sum2[1], s2, s3);
-        f2_unpack(sum2[2], s4, s5);
-        f2_unpack(sum2[3], s6, s7);
-        l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
+        l = l * alpha + sum;
         if (__any_sync(0xffffffffu, resc)) {
           // S_x(j) complete => P V of tile j-1 complete: O_x is stable
 #pragma unroll

@@ -6,20 +6,22 @@
 // which is exact in real arithmetic and equal to applying the pairwise form in ring order.
 // Partials with lse = -inf saw no key: they get weight 0 and their out is never read.
 //
-// HBM-bound: each thread owns one float4 of a D-vector, so a warp reads 512 contiguous bytes of
-// each partial for D = 128 and the LSE loads of a vector are warp-uniform broadcasts.
+// HBM-bound: each thread owns float4 slots of D-vectors (a warp reads 512 contiguous bytes of each
+// partial for D = 128; the LSE loads of a vector are warp-uniform broadcasts).  The partial count
+// is a template parameter so that all loads of an iteration are issued before any is used.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace usp {
 namespace {
 
-constexpr int kMaxParts = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <bool OUT_BF16>
-__global__ void __launch_bounds__(256) lse_merge_kernel(int n_parts, const float* __restrict__ o_parts,
+// NP partials, U vectors' worth of float4 slots per thread per iteration: all LSE loads first,
+// then every needed partial load, so that 2 x NP independent 16-byte loads are in flight.
+template <int NP, bool OUT_BF16, int U>
+__global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict__ o_parts,
                                                         long long o_stride,
                                                         const float* __restrict__ lse_parts,
                                                         long long lse_stride, long long n_vec,
@@ -27,50 +29,80 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(int n_parts, const float
                                                         float* __restrict__ lse_out) {
   const int qpv = D >> 2;  // float4 per vector
   const long long total = n_vec * qpv;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long vec = i / qpv;
-    const int q = static_cast<int>(i - vec * qpv);
-    float l[kMaxParts];
-    float m = -INFINITY;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
+       base += stride * U) {
+    long long vec[U];
+    int q[U];
+    bool valid[U];
+    float l[U][NP];
 #pragma unroll
-    for (int k = 0; k < kMaxParts; ++k) {
-      if (k < n_parts) {
-        l[k] = __ldg(lse_parts + k * lse_stride + vec);
-        m = fmaxf(m, l[k]);
-      }
+    for (int u = 0; u < U; ++u) {
+      const long long i = base + u * stride;
+      valid[u] = i < total;
+      vec[u] = valid[u] ? i / qpv : 0;
+      q[u] = static_cast<int>(i - vec[u] * qpv);
+#pragma unroll
+      for (int k = 0; k < NP; ++k)
+        l[u][k] = valid[u] ? __ldg(lse_parts + k * lse_stride + vec[u]) : -INFINITY;
     }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lse = -INFINITY;
-    if (m != -INFINITY) {
-      float den = 0.f;
+    float4 o[U][NP];
 #pragma unroll
-      for (int k = 0; k < kMaxParts; ++k) {
-        if (k < n_parts && l[k] != -INFINITY) {
-          const float w = ex2_approx((l[k] - m) * kLog2e);
-          const float4 o = __ldcs(reinterpret_cast<const float4*>(o_parts + k * o_stride + vec * D) + q);
-          den += w;
-          acc.x = fmaf(w, o.x, acc.x);
-          acc.y = fmaf(w, o.y, acc.y);
-          acc.z = fmaf(w, o.z, acc.z);
-          acc.w = fmaf(w, o.w, acc.w);
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int k = 0; k < NP; ++k)
+        if (l[u][k] != -INFINITY)
+          o[u][k] = __ldcs(reinterpret_cast<const float4*>(o_parts + k * o_stride + vec[u] * D) + q[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!valid[u]) continue;
+      float m = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < NP; ++k) m = fmaxf(m, l[u][k]);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float lse = -INFINITY;
+      if (m != -INFINITY) {
+        float den = 0.f;
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+          if (l[u][k] != -INFINITY) {
+            const float w = ex2_approx((l[u][k] - m) * kLog2e);
+            den += w;
+            acc.x = fmaf(w, o[u][k].x, acc.x);
+            acc.y = fmaf(w, o[u][k].y, acc.y);
+            acc.z = fmaf(w, o[u][k].z, acc.z);
+            acc.w = fmaf(w, o[u][k].w, acc.w);
+          }
         }
+        const float inv = 1.0f / den;
+        acc.x *= inv;
+        acc.y *= inv;
+        acc.z *= inv;
+        acc.w *= inv;
+        lse = m + lg2_approx(den) * kLn2;
       }
-      const float inv = 1.0f / den;
-      acc.x *= inv;
-      acc.y *= inv;
-      acc.z *= inv;
-      acc.w *= inv;
-      lse = m + lg2_approx(den) * kLn2;
+      if (OUT_BF16) {
+        const uint2 packed = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        reinterpret_cast<uint2*>(static_cast<char*>(o_out) + (vec[u] * D) * 2)[q[u]] = packed;
+      } else {
+        reinterpret_cast<float4*>(static_cast<float*>(o_out) + vec[u] * D)[q[u]] = acc;
+      }
+      if (q[u] == 0 && lse_out) lse_out[vec[u]] = lse;
     }
-    if (OUT_BF16) {
-      uint2 packed = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-      reinterpret_cast<uint2*>(static_cast<char*>(o_out) + (vec * D) * 2)[q] = packed;
-    } else {
-      reinterpret_cast<float4*>(static_cast<float*>(o_out) + vec * D)[q] = acc;
-    }
-    if (q == 0 && lse_out) lse_out[vec] = lse;
   }
+}
+
+template <int NP>
+void launch_np(bool out_bf16, unsigned blocks, cudaStream_t stream, const float* o_parts,
+               long long o_stride, const float* lse_parts, long long lse_stride, long long n_vec,
+               int D, void* o_out, float* lse_out) {
+  constexpr int U = NP <= 4 ? 2 : 1;
+  if (out_bf16)
+    lse_merge_kernel<NP, true, U><<<blocks, 256, 0, stream>>>(o_parts, o_stride, lse_parts,
+                                                              lse_stride, n_vec, D, o_out, lse_out);
+  else
+    lse_merge_kernel<NP, false, U><<<blocks, 256, 0, stream>>>(o_parts, o_stride, lse_parts,
+                                                               lse_stride, n_vec, D, o_out, lse_out);
 }
 
 }  // namespace
@@ -83,12 +115,21 @@ usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_
   const long long total = n_vec * (D / 4);
   long long blocks = (total + 255) / 256;
   if (blocks > 152LL * 16) blocks = 152LL * 16;
-  if (out_bf16)
-    lse_merge_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        n_parts, o_parts, o_part_stride, lse_parts, lse_part_stride, n_vec, D, o_out, lse_out);
-  else
-    lse_merge_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        n_parts, o_parts, o_part_stride, lse_parts, lse_part_stride, n_vec, D, o_out, lse_out);
+  const unsigned nb = static_cast<unsigned>(blocks);
+#define USP_MERGE_CASE(N)                                                                        \
+  case N:                                                                                        \
+    launch_np<N>(out_bf16, nb, stream, o_parts, o_part_stride, lse_parts, lse_part_stride, n_vec, \
+                 D, o_out, lse_out);                                                             \
+    break;
+  switch (n_parts) {
+    USP_MERGE_CASE(1) USP_MERGE_CASE(2) USP_MERGE_CASE(3) USP_MERGE_CASE(4) USP_MERGE_CASE(5)
+    USP_MERGE_CASE(6) USP_MERGE_CASE(7) USP_MERGE_CASE(8) USP_MERGE_CASE(9) USP_MERGE_CASE(10)
+    USP_MERGE_CASE(11) USP_MERGE_CASE(12) USP_MERGE_CASE(13) USP_MERGE_CASE(14)
+    USP_MERGE_CASE(15) USP_MERGE_CASE(16)
+    default:
+      return fail(USP_ERR_INVALID_ARG, "n_parts %d outside [1, 16]", n_parts);
+  }
+#undef USP_MERGE_CASE
   return check_launch("lse merge kernel");
 }
 
