@@ -186,17 +186,54 @@ def workload(name: str):
 
 
 def phase_bytes(w, out_elem: int):
-    """Algorithmic HBM bytes of the bandwidth-bound phases (each element read once + written once)."""
+    """Algorithmic HBM bytes of the bandwidth-bound phases (each element read once + written once).
+
+    Q/K/V are re-laid by a separate pass only for zigzag order with several ring ranks (otherwise
+    the attention's tensor maps address each virtual rank's head-sharded view in place); O and LSE
+    are always written in the global layout by the attention (one ring rank) or the merge."""
     elems = w.B * w.S * w.H * w.D
     rows_h = w.B * w.S * w.H
-    relayout = not (w.ulysses_degree == 1 and (w.ring_degree == 1 or (w.order == "contiguous" and w.B == 1)))
-    b = {"qkv_relayout": 2 * 3 * elems * 2 if relayout else 0}
+    qkv_pass = w.order == "zigzag" and w.ring_degree > 1
+    b = {"qkv_relayout": 2 * 3 * elems * 2 if qkv_pass else 0}
     if w.ring_degree > 1:
         b["merge"] = w.ring_degree * (elems * 4 + rows_h * 4) + elems * out_elem + rows_h * 4
     else:
         b["merge"] = 0
-    b["out_relayout"] = 2 * (elems * out_elem + rows_h * 4) if relayout else 0
     return b
+
+
+def standalone_relayout(w, q, k, v, o, flush, stream, reps: int = 50):
+    """GB/s of the standalone Ulysses re-layout entry points on this workload's tensors: seq->head
+    of Q, K, V and head->seq of O over the Ulysses split (a separately timed measurement, since the
+    end-to-end step addresses these layouts in place)."""
+    import torch
+
+    from sequence_attention_tcgen05_gb300 import usp
+    U = max(2, w.ulysses_degree)
+    lens = [w.S // U + (1 if p < w.S % U else 0) for p in range(U)]
+    outs = [torch.empty_like(x) for x in (q, k, v)]
+    oo = torch.empty_like(o)
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    t_in = t_out = 0.0
+    for i in range(reps + 3):
+        flush.zero_()
+        e0.record(stream)
+        for x, y in zip((q, k, v), outs):
+            usp.usp_relayout_seq2head(x, y, w.B, w.H, w.D, lens, stream=stream)
+        e1.record(stream)
+        usp.usp_relayout_head2seq(o, oo, w.B, w.H, w.D, lens, stream=stream)
+        e2.record(stream)
+        e2.synchronize()
+        if i >= 3:
+            t_in += e0.elapsed_time(e1)
+            t_out += e1.elapsed_time(e2)
+    elems = w.B * w.S * w.H * w.D
+    bin_, bout = 2 * 3 * elems * 2, 2 * elems * o.element_size()
+    return {"ulysses_split": lens,
+            "seq2head_qkv": {"GB/s": bin_ / (t_in / reps / 1e3) / 1e9, "bytes": bin_,
+                             "us": t_in / reps * 1e3},
+            "head2seq_o": {"GB/s": bout / (t_out / reps / 1e3) / 1e9, "bytes": bout,
+                           "us": t_out / reps * 1e3}}
 
 
 def cpu_oracle_sample(w, target_s: float, rng_seed: int = 0):
@@ -387,14 +424,18 @@ def run_ours(args):
     traffic_bytes = traffic["bytes"] if traffic and traffic["kernel_hash"] == kernel_hash() else None
     pb = phase_bytes(w, out_elem)
     bw = {}
-    for name in ("qkv_relayout", "merge", "out_relayout"):
+    for name in ("qkv_relayout", "merge"):
         if pb[name]:
             s = phases[name] / 1000.0 / args.steps
             gbs = pb[name] / s / 1e9
             bw[name] = {"GB/s": gbs, "bytes": pb[name], "us": s * 1e6,
                         "frac_measured_hbm": gbs / peaks["hbm_gbs"], "frac_8TBs": gbs / NOMINAL_HBM_GBS}
     bw_bytes = sum(pb.values())
-    bw_s = sum(phases[n] for n in ("qkv_relayout", "merge", "out_relayout")) / 1000.0 / args.steps
+    standalone = standalone_relayout(w, q, k, v, o, flush, stream)
+    for part in ("seq2head_qkv", "head2seq_o"):
+        standalone[part]["frac_measured_hbm"] = standalone[part]["GB/s"] / peaks["hbm_gbs"]
+        standalone[part]["frac_8TBs"] = standalone[part]["GB/s"] / NOMINAL_HBM_GBS
+    bw_s = sum(phases[n] for n in ("qkv_relayout", "merge")) / 1000.0 / args.steps
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -409,7 +450,7 @@ def run_ours(args):
         "relayout_merge": {"GB/s": bw_bytes / bw_s / 1e9 if bw_s > 0 else None,
                            "frac_measured_hbm": (bw_bytes / bw_s / 1e9 / peaks["hbm_gbs"]) if bw_s > 0 else None,
                            "frac_8TBs": (bw_bytes / bw_s / 1e9 / NOMINAL_HBM_GBS) if bw_s > 0 else None,
-                           "phases": bw},
+                           "phases": bw, "standalone_relayout": standalone},
         "phases_ms_per_step": {k: v / args.steps for k, v in phases.items()},
         "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

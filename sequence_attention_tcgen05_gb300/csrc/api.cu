@@ -182,12 +182,14 @@ struct Grid {
   std::vector<Positions> pos;  // per ring group
   std::vector<int> S_r;        // ring chunk lengths
   std::vector<int> h, hoff;    // head groups
-  bool relayout = false;       // Q/K/V and O need the head-sharded workspace copies
+  // Q/K/V of every virtual rank can be addressed in place in the global tensor (each ring chunk is
+  // one affine run of rows); otherwise (zigzag with several ring ranks) they are first re-laid into
+  // the head-sharded workspace copies.
+  bool fused_in = true;
   // workspace layout (bytes)
-  size_t off_q = 0, off_k = 0, off_v = 0, off_opart = 0, off_lpart = 0, off_wo = 0, off_wl = 0,
-         total = 0;
+  size_t off_q = 0, off_k = 0, off_v = 0, off_opart = 0, off_lpart = 0, total = 0;
   int64_t elems = 0;  // B*S*H*D
-  int64_t woff(int r, int u, int d) const {  // element offset of block (r, u) in W layout
+  int64_t woff(int r, int u, int d) const {  // element offset of block (r, u) in the W layout
     int64_t off = 0;
     for (int rr = 0; rr < r; ++rr) off += int64_t(B) * S_r[rr] * H * d;
     for (int uu = 0; uu < u; ++uu) off += int64_t(B) * S_r[r] * h[uu] * d;
@@ -235,17 +237,16 @@ usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int U, int R, usp_o
   }
   g.hoff.assign(U, 0);
   for (int u = 1; u < U; ++u) g.hoff[u] = g.hoff[u - 1] + g.h[u - 1];
-  g.relayout = !(U == 1 && (R == 1 || (order == USP_ORDER_CONTIGUOUS && B == 1)));
+  g.fused_in = order != USP_ORDER_ZIGZAG || R == 1;
   g.elems = int64_t(B) * S * H * D;
   const int64_t rowsH = int64_t(B) * S * H;
-  const size_t oel = o_dt == USP_BF16 ? 2 : 4;
   size_t at = 256;  // status word
   auto take = [&](size_t bytes) {
     const size_t o = at;
     at = static_cast<size_t>(align_up(static_cast<int64_t>(at + bytes), 256));
     return o;
   };
-  if (g.relayout) {
+  if (!g.fused_in) {
     g.off_q = take(g.elems * 2);
     g.off_k = take(g.elems * 2);
     g.off_v = take(g.elems * 2);
@@ -253,10 +254,6 @@ usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int U, int R, usp_o
   if (R > 1) {
     g.off_opart = take(size_t(R) * g.elems * 4);
     g.off_lpart = take(size_t(R) * rowsH * 4);
-  }
-  if (g.relayout) {
-    g.off_wo = take(g.elems * oel);
-    g.off_wl = take(rowsH * 4);
   }
   g.total = at;
   return USP_OK;
@@ -418,9 +415,9 @@ usp_status_t usp_attn_partial(const void* q, const void* k, const void* v, int B
   AttnParams& p = params;
   std::memset(&p, 0, sizeof(p));
   usp_status_t st;
-  if ((st = make_qkv_map(&p.maps[0], q, H, D, int64_t(B) * Sq, q_row_stride))) return st;
-  if ((st = make_qkv_map(&p.maps[1], k, H, D, int64_t(B) * Sk, kv_row_stride))) return st;
-  if ((st = make_qkv_map(&p.maps[2], v, H, D, int64_t(B) * Sk, kv_row_stride))) return st;
+  if ((st = make_qkv_map(&p.maps[0], q, H, D, Sq, B, q_row_stride, int64_t(Sq) * q_row_stride))) return st;
+  if ((st = make_qkv_map(&p.maps[1], k, H, D, Sk, B, kv_row_stride, int64_t(Sk) * kv_row_stride))) return st;
+  if ((st = make_qkv_map(&p.maps[2], v, H, D, Sk, B, kv_row_stride, int64_t(Sk) * kv_row_stride))) return st;
   p.B = B;
   p.o_bf16 = o_dt == USP_BF16;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -445,10 +442,11 @@ usp_status_t usp_attn_partial(const void* q, const void* k, const void* v, int B
     AttnSeg s{};
     s.o = o; s.lse = lse;
     s.q_map = 0; s.k_map = 1; s.v_map = 2;
-    s.q_row0 = r.q0; s.q_bstride = Sq; s.q_len = r.q_len;
-    s.kv_row0 = 0; s.kv_bstride = Sk; s.kv_len = r.kv_len;
+    s.q_row0 = r.q0; s.q_len = r.q_len;
+    s.kv_row0 = 0; s.kv_len = r.kv_len;
     s.diag = r.diag; s.n_heads = H;
-    s.o_row0 = r.q0; s.o_bstride = Sq;
+    s.o_row0 = r.q0; s.o_bstride = Sq; s.o_heads = H;
+    s.o_start0 = 0; s.o_len0 = INT_MAX; s.o_start1 = 0; s.o_stride = 1;
     s.rev = q_pos != nullptr;
     segs.push_back(s);
   }
@@ -471,7 +469,8 @@ usp_status_t usp_lse_merge(int n_parts, const float* o_parts, int64_t o_part_str
   if (n_rows == 0) return USP_OK;
   if (usp_status_t st = check_device()) return st;
   return launch_lse_merge(n_parts, o_parts, o_part_stride, lse_parts, lse_part_stride, n_rows * H, D,
-                          o_out, out_dt == USP_BF16, lse_out, reinterpret_cast<cudaStream_t>(stream));
+                          o_out, out_dt == USP_BF16, lse_out, nullptr,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t usp_attention_workspace_size(int B, int S, int H, int D, int ulysses_degree,
@@ -516,11 +515,10 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
   const int oel = o_dt == USP_BF16 ? 2 : 4;
   usp_status_t st;
 
-  // 1. fused reorder + seq -> head re-layout of Q, K, V into the head-sharded W layout
-  const void* wq = q;
-  const void* wk = k;
-  const void* wv = v;
-  if (g.relayout) {
+  // 1. Q, K, V of virtual rank (r, u): in place in the global tensor when ring chunk r is one affine
+  //    run of rows (the head-sharded view is then pure addressing); otherwise a fused reorder +
+  //    seq -> head re-layout into the workspace first.
+  if (!g.fused_in) {
     RelayoutParams rp;
     fill_relayout_grid(rp, g, D, 2);
     rp.n_tensors = 3;
@@ -530,7 +528,6 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     rp.dir = 0;
     if ((st = launch_relayout(rp, stream))) return st;
     ++launches;
-    wq = ws + g.off_q; wk = ws + g.off_k; wv = ws + g.off_v;
   }
   if ((st = mark(1))) return st;
 
@@ -541,34 +538,37 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
   auto map_index = [&](int r, int u, int t) { return (r * U + u) * 3 + t; };
   for (int r = 0; r < R; ++r) {
     for (int u = 0; u < U; ++u) {
-      const int64_t off = g.woff(r, u, D) * 2;  // bytes
-      const int64_t rows = int64_t(B) * g.S_r[r];
-      const int64_t stride = int64_t(g.h[u]) * D;
-      if ((st = make_qkv_map(&p.maps[map_index(r, u, 0)], static_cast<const char*>(wq) + off, g.h[u], D, rows, stride))) return st;
-      if ((st = make_qkv_map(&p.maps[map_index(r, u, 1)], static_cast<const char*>(wk) + off, g.h[u], D, rows, stride))) return st;
-      if ((st = make_qkv_map(&p.maps[map_index(r, u, 2)], static_cast<const char*>(wv) + off, g.h[u], D, rows, stride))) return st;
+      const void* base[3];
+      int64_t row_stride, batch_stride;
+      if (g.fused_in) {
+        const int64_t e0 = (int64_t(g.pos[r].start[0]) * H + g.hoff[u]) * D;
+        base[0] = static_cast<const uint16_t*>(q) + e0;
+        base[1] = static_cast<const uint16_t*>(k) + e0;
+        base[2] = static_cast<const uint16_t*>(v) + e0;
+        row_stride = int64_t(g.pos[r].stride) * H * D;
+        batch_stride = int64_t(S) * H * D;
+      } else {
+        const int64_t off = g.woff(r, u, D) * 2;
+        base[0] = ws + g.off_q + off;
+        base[1] = ws + g.off_k + off;
+        base[2] = ws + g.off_v + off;
+        row_stride = int64_t(g.h[u]) * D;
+        batch_stride = int64_t(g.S_r[r]) * row_stride;
+      }
+      if (B == 1) batch_stride = std::max<int64_t>(1, g.S_r[r]) * row_stride;
+      for (int t = 0; t < 3; ++t)
+        if ((st = make_qkv_map(&p.maps[map_index(r, u, t)], base[t], g.h[u], D, g.S_r[r], B, row_stride,
+                               batch_stride)))
+          return st;
     }
   }
   p.B = B;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.budget_ns = wait_budget_ns();
-  // where the attention writes: ring partials (fp32) when R > 1, else the final O (o_dt)
-  char* att_o;
-  float* att_l;
-  int64_t slot_o = 0, slot_l = 0;
-  if (R > 1) {
-    att_o = ws + g.off_opart;
-    att_l = reinterpret_cast<float*>(ws + g.off_lpart);
-    slot_o = g.elems * 4;
-    slot_l = int64_t(B) * S * H;
-    p.o_bf16 = 0;
-  } else {
-    att_o = g.relayout ? ws + g.off_wo : static_cast<char*>(o);
-    att_l = g.relayout ? reinterpret_cast<float*>(ws + g.off_wl) : lse;
-    p.o_bf16 = o_dt == USP_BF16;
-  }
-  const int oel_att = p.o_bf16 ? 2 : 4;
+  // ring partials (fp32, head-sharded W layout) when R > 1; else the final output in place
+  const int64_t slot_o = g.elems * 4, slot_l = int64_t(B) * S * H;
+  p.o_bf16 = R > 1 ? 0 : (o_dt == USP_BF16);
   std::vector<AttnSeg> segs;
   for (int r = 0; r < R; ++r) {
     for (int kstep = 0; kstep < R; ++kstep) {
@@ -577,16 +577,26 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
       for (int u = 0; u < U; ++u) {
         for (const Run& run : runs) {
           AttnSeg s{};
-          s.o = att_o + kstep * slot_o + g.woff(r, u, D) * oel_att;
-          s.lse = att_l ? att_l + kstep * slot_l + g.woff(r, u, 1) : nullptr;
           s.q_map = map_index(r, u, 0);
           s.k_map = map_index(r2, u, 1);
           s.v_map = map_index(r2, u, 2);
-          s.q_row0 = run.q0; s.q_bstride = g.S_r[r]; s.q_len = run.q_len;
-          s.kv_row0 = 0; s.kv_bstride = g.S_r[r2]; s.kv_len = run.kv_len;
+          s.q_row0 = run.q0; s.q_len = run.q_len;
+          s.kv_row0 = 0; s.kv_len = run.kv_len;
           s.diag = run.diag; s.n_heads = g.h[u];
-          s.o_row0 = run.q0; s.o_bstride = g.S_r[r];
+          s.o_row0 = run.q0;
           s.rev = causal != 0;
+          if (R > 1) {
+            s.o = ws + g.off_opart + kstep * slot_o + g.woff(r, u, D) * 4;
+            s.lse = reinterpret_cast<float*>(ws + g.off_lpart) + kstep * slot_l + g.woff(r, u, 1);
+            s.o_bstride = g.S_r[r]; s.o_heads = g.h[u];
+            s.o_start0 = 0; s.o_len0 = INT_MAX; s.o_start1 = 0; s.o_stride = 1;
+          } else {
+            s.o = static_cast<char*>(o) + int64_t(g.hoff[u]) * D * oel;
+            s.lse = lse ? lse + g.hoff[u] : nullptr;
+            s.o_bstride = S; s.o_heads = H;
+            s.o_start0 = g.pos[r].start[0]; s.o_len0 = g.pos[r].n_seg > 1 ? g.pos[r].len[0] : INT_MAX;
+            s.o_start1 = g.pos[r].start[1]; s.o_stride = g.pos[r].stride;
+          }
           segs.push_back(s);
         }
       }
@@ -596,38 +606,37 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
   launches += static_cast<int>((segs.size() + kAttnMaxSegs - 1) / kAttnMaxSegs);
   if ((st = mark(2))) return st;
 
-  // 3. merge the ring partials
-  char* fin_o = g.relayout ? ws + g.off_wo : static_cast<char*>(o);
-  float* fin_l = g.relayout ? reinterpret_cast<float*>(ws + g.off_wl) : lse;
+  // 3. merge the ring partials straight into the global layout (the head -> seq all-to-all and the
+  //    inverse reorder are the merge's store addressing)
   if (R > 1) {
+    MergeMap mm;
+    std::memset(&mm, 0, sizeof(mm));
+    mm.n_blocks = R * U;
+    mm.H = H;
+    mm.S = S;
+    for (int r = 0; r < R; ++r) {
+      for (int u = 0; u < U; ++u) {
+        const int kb = r * U + u;
+        mm.vec0[kb] = g.woff(r, u, 1);
+        mm.row0[kb] = kb == 0 ? 0 : mm.row0[kb - 1] + int64_t(B) * g.S_r[(kb - 1) / U];
+        mm.S_r[kb] = std::max(1, g.S_r[r]);
+        mm.h[kb] = g.h[u];
+        mm.hoff[kb] = g.hoff[u];
+        mm.p_start0[kb] = g.pos[r].start[0];
+        mm.p_len0[kb] = g.pos[r].n_seg > 1 ? g.pos[r].len[0] : INT_MAX;
+        mm.p_start1[kb] = g.pos[r].start[1];
+        mm.p_stride[kb] = g.pos[r].stride;
+      }
+    }
+    mm.vec0[R * U] = int64_t(B) * S * H;
+    mm.row0[R * U] = mm.row0[R * U - 1] + int64_t(B) * g.S_r[R - 1];
     if ((st = launch_lse_merge(R, reinterpret_cast<const float*>(ws + g.off_opart), g.elems,
                                reinterpret_cast<const float*>(ws + g.off_lpart), int64_t(B) * S * H,
-                               int64_t(B) * S * H, D, fin_o, o_dt == USP_BF16, fin_l, stream)))
+                               int64_t(B) * S * H, D, o, o_dt == USP_BF16, lse, &mm, stream)))
       return st;
     ++launches;
   }
   if ((st = mark(3))) return st;
-
-  // 4. fused head -> seq re-layout + inverse reorder of O and LSE
-  if (g.relayout) {
-    RelayoutParams rp;
-    fill_relayout_grid(rp, g, D, oel);
-    rp.n_tensors = 1;
-    rp.src[0] = ws + g.off_wo;
-    rp.dst[0] = static_cast<char*>(o);
-    rp.dir = 1;
-    if ((st = launch_relayout(rp, stream))) return st;
-    ++launches;
-    if (lse) {
-      fill_relayout_grid(rp, g, 1, 4);
-      rp.n_tensors = 1;
-      rp.src[0] = ws + g.off_wl;
-      rp.dst[0] = reinterpret_cast<char*>(lse);
-      rp.dir = 1;
-      if ((st = launch_relayout(rp, stream))) return st;
-      ++launches;
-    }
-  }
   if ((st = mark(4))) return st;
   if (n_launches) *n_launches = launches;
   return USP_OK;

@@ -214,28 +214,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const AttnSeg& s = *u.seg;
         if (q_iter > 0 && !mbar_wait(q_empty, (q_iter - 1) & 1, abort_flag, p.status, budget)) break;
         mbar_arrive_expect_tx(q_full, 2 * L::kQTile);
-        const int qrow = s.q_row0 + u.b * s.q_bstride + u.q0;
+        const int qrow = s.q_row0 + u.q0;
 #pragma unroll
         for (int x = 0; x < 2; ++x)
 #pragma unroll
           for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_3d(sm + L::kQ + x * L::kQTile + blk * kAttnBM * 128, &p.maps[s.q_map], blk * 64,
-                        u.h, qrow + x * kAttnBM, q_full);
+            tma_load_4d(sm + L::kQ + x * L::kQTile + blk * kAttnBM * 128, &p.maps[s.q_map], blk * 64,
+                        u.h, qrow + x * kAttnBM, u.b, q_full);
         ++q_iter;
-        const int kvrow = s.kv_row0 + u.b * s.kv_bstride;
+        const int kvrow = s.kv_row0;
         bool ok = true;
         for (int j = 0; j < u.n_kv; ++j) {
           if (!mbar_wait(&kv_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
           mbar_arrive_expect_tx(&k_full[stage], L::kKBytes);
 #pragma unroll
           for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_3d(sm + L::kK + stage * L::kKBytes + blk * kAttnBN * 128, &p.maps[s.k_map],
-                        blk * 64, u.h, kvrow + j * kAttnBN, &k_full[stage]);
+            tma_load_4d(sm + L::kK + stage * L::kKBytes + blk * kAttnBN * 128, &p.maps[s.k_map],
+                        blk * 64, u.h, kvrow + j * kAttnBN, u.b, &k_full[stage]);
           mbar_arrive_expect_tx(&v_full[stage], L::kVBytes);
 #pragma unroll
           for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_3d(sm + L::kV + stage * L::kVBytes + blk * kAttnBN * 128, &p.maps[s.v_map],
-                        blk * 64, u.h, kvrow + j * kAttnBN, &v_full[stage]);
+            tma_load_4d(sm + L::kV + stage * L::kVBytes + blk * kAttnBN * 128, &p.maps[s.v_map],
+                        blk * 64, u.h, kvrow + j * kAttnBN, u.b, &v_full[stage]);
           ++fills[stage];
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -339,8 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const AttnSeg& s = *u.seg;
       const int q0 = u.q0 + x * kAttnBM;  // first local row of this query tile
       const bool row_valid = row < u.qv[x];
-      const long long orow = static_cast<long long>(u.b) * s.o_bstride + s.o_row0 + q0 + row;
-      const long long o_elem = (orow * s.n_heads + u.h) * D;
+      const int ol = s.o_row0 + q0 + row;  // output-side local row
+      const long long opos = ol < s.o_len0
+                                 ? static_cast<long long>(s.o_start0) + static_cast<long long>(ol) * s.o_stride
+                                 : static_cast<long long>(s.o_start1) + static_cast<long long>(ol - s.o_len0) * s.o_stride;
+      const long long orow = static_cast<long long>(u.b) * s.o_bstride + opos;
+      const long long o_elem = (orow * s.o_heads + u.h) * D;
       if (u.n_kv == 0) {
         if (row_valid) {
           if (p.o_bf16) {
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(s.o) + o_elem);
             for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          if (s.lse) s.lse[orow * s.n_heads + u.h] = -INFINITY;
+          if (s.lse) s.lse[orow * s.o_heads + u.h] = -INFINITY;
         }
         continue;
       }
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       }
       if (row_valid) {
-        if (s.lse) s.lse[orow * s.n_heads + u.h] = lse;
+        if (s.lse) s.lse[orow * s.o_heads + u.h] = lse;
       }
     }
   }
@@ -486,7 +490,7 @@ usp_status_t launch_one(const AttnParams& p, cudaStream_t stream) {
 }  // namespace
 
 usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D, int64_t rows,
-                          int64_t row_stride) {
+                          int B, int64_t row_stride, int64_t batch_stride) {
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -501,13 +505,15 @@ usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D
     return reinterpret_cast<EncodeFn>(fn);
   }();
   if (!encode) return fail(USP_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(n_heads),
-                              static_cast<cuuint64_t>(std::max<int64_t>(rows, 1))};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                                 static_cast<cuuint64_t>(row_stride) * 2};
-  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kAttnBM)};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(n_heads),
+                              static_cast<cuuint64_t>(std::max<int64_t>(rows, 1)),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(row_stride) * 2,
+                                 static_cast<cuuint64_t>(std::max<int64_t>(batch_stride, row_stride)) * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kAttnBM), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -74,10 +74,24 @@ usp_status_t launch_relayout(RelayoutParams& p, cudaStream_t stream);
 // ------------------------------------------------------------------------------------------
 // LSE merge.
 // ------------------------------------------------------------------------------------------
+// Optional output placement for the merge: the partials are in the head-sharded layout of
+// usp_attention (blocks (r, u) of [B][S_r][h_u] vectors, back to back); the merged vector of block k,
+// batch b, ring-local row l, head h' goes to global row b*S + pos_k(l), head hoff_k + h'.
+constexpr int kMergeMaxBlocks = 16;
+struct MergeMap {
+  int n_blocks;
+  int H, S;
+  long long vec0[kMergeMaxBlocks + 1];  // first vector of each block; vec0[n_blocks] = total
+  long long row0[kMergeMaxBlocks + 1];  // first row (B * S_r rows per block); row0[n_blocks] = total
+  int S_r[kMergeMaxBlocks], h[kMergeMaxBlocks], hoff[kMergeMaxBlocks];
+  int p_start0[kMergeMaxBlocks], p_len0[kMergeMaxBlocks], p_start1[kMergeMaxBlocks],
+      p_stride[kMergeMaxBlocks];
+};
+
 usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_stride,
                               const float* lse_parts, int64_t lse_part_stride, int64_t n_vec,
                               int D, void* o_out, bool out_bf16, float* lse_out,
-                              cudaStream_t stream);
+                              const MergeMap* map, cudaStream_t stream);
 
 // ------------------------------------------------------------------------------------------
 // Partial attention (tcgen05).
@@ -91,19 +105,25 @@ constexpr int kNoDiag = INT_MAX;
 
 // One run of query rows against one key range: key c (0 <= c < kv_len) is visible to local
 // query row i (0 <= i < q_len) iff c <= i + diag (diag == kNoDiag: no limit).
+// Q/K/V tiles come from 4-D tensor maps {D, heads, rows, batch}; rows of this run are map rows
+// q_row0 + i (and kv_row0 + c).  Output row of query i of batch b:
+//   row = b * o_bstride + pos(o_row0 + i),  pos(l) = l < o_len0 ? o_start0 + l * o_stride
+//                                                               : o_start1 + (l - o_len0) * o_stride
+// and element (row * o_heads + h) * D of `o` (LSE: row * o_heads + h of `lse`); `o` and `lse` are
+// already offset to the run's first head.  Identity pos (o_len0 = INT_MAX) for a dense output.
 struct AttnSeg {
-  void* o;        // output block base (fp32 or bf16 per launch): rows [B][o_bstride], heads n_heads
-  float* lse;     // LSE block base (may be null)
+  void* o;        // fp32 or bf16 per launch
+  float* lse;     // may be null
   int q_map, k_map, v_map;
-  int q_row0, q_bstride, q_len;
-  int kv_row0, kv_bstride, kv_len;
+  int q_row0, q_len;
+  int kv_row0, kv_len;
   int diag;
-  int n_heads;
-  int o_row0, o_bstride;
-  int n_qblk;     // 256-row query blocks (work units per batch and head)
+  int n_heads;    // heads of the maps (work units per batch = n_qblk * n_heads)
+  int o_row0, o_bstride, o_heads;
+  int o_start0, o_len0, o_start1, o_stride;
+  int n_qblk;     // 256-row query blocks
   int unit0;
   int rev;        // 1: visit query blocks last first (causal: longest first)
-  int pad;
 };
 
 struct AttnParams {
@@ -126,9 +146,10 @@ struct Run {
 // causal = false gives one run covering everything.
 std::vector<Run> plan_runs(const Positions& qp, const Positions& kp, bool causal);
 
-// Tensor map over a bf16 buffer of `rows` rows x `n_heads` heads x D, row stride in elements.
+// 4-D tensor map {D, n_heads, rows, B} over bf16 data: heads adjacent (D elements apart), rows
+// row_stride elements apart, batches batch_stride elements apart.
 usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D, int64_t rows,
-                          int64_t row_stride);
+                          int B, int64_t row_stride, int64_t batch_stride);
 
 // Launch over all segments (split into several launches if there are more than fit).
 usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs, int D,

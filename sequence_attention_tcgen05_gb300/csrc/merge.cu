@@ -9,6 +9,8 @@
 // HBM-bound: each thread owns float4 slots of D-vectors (a warp reads 512 contiguous bytes of each
 // partial for D = 128; the LSE loads of a vector are warp-uniform broadcasts).  The partial count
 // is a template parameter so that all loads of an iteration are issued before any is used.
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -81,22 +83,131 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
         acc.w *= inv;
         lse = m + lg2_approx(den) * kLn2;
       }
+      const long long ov = vec[u];
       if (OUT_BF16) {
         const uint2 packed = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-        reinterpret_cast<uint2*>(static_cast<char*>(o_out) + (vec[u] * D) * 2)[q[u]] = packed;
+        reinterpret_cast<uint2*>(static_cast<char*>(o_out) + (ov * D) * 2)[q[u]] = packed;
       } else {
-        reinterpret_cast<float4*>(static_cast<float*>(o_out) + vec[u] * D)[q[u]] = acc;
+        reinterpret_cast<float4*>(static_cast<float*>(o_out) + ov * D)[q[u]] = acc;
       }
-      if (q[u] == 0 && lse_out) lse_out[vec[u]] = lse;
+      if (q[u] == 0 && lse_out) lse_out[ov] = lse;
+    }
+  }
+}
+
+
+// Merge with the result placed in the global layout (MergeMap): one warp per token row of one
+// head-sharded block, i.e. h_u contiguous D-vectors on both sides.  The row's placement is decoded
+// once; the lanes then stream the row's h_u * D / 4 float4 slots, four at a time, issuing the
+// partials' loads of a batch before combining them.
+template <int NP, bool OUT_BF16>
+__global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __restrict__ o_parts,
+                                                             long long o_stride,
+                                                             const float* __restrict__ lse_parts,
+                                                             long long lse_stride, int D,
+                                                             void* __restrict__ o_out,
+                                                             float* __restrict__ lse_out,
+                                                             const __grid_constant__ MergeMap m) {
+  constexpr int kB = 4;
+  const int lane = threadIdx.x & 31;
+  const long long total = m.row0[m.n_blocks];
+  const long long step = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const int qpv = D >> 2;
+  for (long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       row < total; row += step) {
+    int lo = 0, hi = m.n_blocks - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (m.row0[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    const long long rr = row - m.row0[lo];
+    const int Sr = m.S_r[lo];
+    const long long b = rr / Sr;
+    const int l = static_cast<int>(rr - b * Sr);
+    const long long pos = l < m.p_len0[lo] ? m.p_start0[lo] + static_cast<long long>(l) * m.p_stride[lo]
+                                           : m.p_start1[lo] + static_cast<long long>(l - m.p_len0[lo]) * m.p_stride[lo];
+    const int hh = m.h[lo];
+    const long long src_vec = m.vec0[lo] + rr * hh;          // W vector of (row, head 0)
+    const long long dst_vec = (b * m.S + pos) * m.H + m.hoff[lo];
+    const int nf4 = hh * qpv;
+    for (int f0 = 0; f0 < nf4; f0 += 32 * kB) {
+      float l_[kB][NP];
+      float4 o_[kB][NP];
+      int head[kB], q[kB];
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        const int f = f0 + i * 32 + lane;
+        head[i] = f / qpv;
+        q[i] = f - head[i] * qpv;
+#pragma unroll
+        for (int k = 0; k < NP; ++k)
+          l_[i][k] = f < nf4 ? __ldg(lse_parts + k * lse_stride + src_vec + head[i]) : -INFINITY;
+      }
+#pragma unroll
+      for (int i = 0; i < kB; ++i)
+#pragma unroll
+        for (int k = 0; k < NP; ++k)
+          if (l_[i][k] != -INFINITY)
+            o_[i][k] = __ldcs(reinterpret_cast<const float4*>(o_parts + k * o_stride +
+                                                              (src_vec + head[i]) * D) + q[i]);
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        if (f0 + i * 32 + lane >= nf4) continue;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NP; ++k) mx = fmaxf(mx, l_[i][k]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lse = -INFINITY;
+        if (mx != -INFINITY) {
+          float den = 0.f;
+#pragma unroll
+          for (int k = 0; k < NP; ++k) {
+            if (l_[i][k] != -INFINITY) {
+              const float w = ex2_approx((l_[i][k] - mx) * kLog2e);
+              den += w;
+              acc.x = fmaf(w, o_[i][k].x, acc.x);
+              acc.y = fmaf(w, o_[i][k].y, acc.y);
+              acc.z = fmaf(w, o_[i][k].z, acc.z);
+              acc.w = fmaf(w, o_[i][k].w, acc.w);
+            }
+          }
+          const float inv = 1.0f / den;
+          acc.x *= inv;
+          acc.y *= inv;
+          acc.z *= inv;
+          acc.w *= inv;
+          lse = mx + lg2_approx(den) * kLn2;
+        }
+        const long long ov = dst_vec + head[i];
+        if (OUT_BF16) {
+          const uint2 packed = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+          reinterpret_cast<uint2*>(static_cast<char*>(o_out) + (ov * D) * 2)[q[i]] = packed;
+        } else {
+          reinterpret_cast<float4*>(static_cast<float*>(o_out) + ov * D)[q[i]] = acc;
+        }
+        if (q[i] == 0 && lse_out) lse_out[ov] = lse;
+      }
     }
   }
 }
 
 template <int NP>
-void launch_np(bool out_bf16, unsigned blocks, cudaStream_t stream, const float* o_parts,
-               long long o_stride, const float* lse_parts, long long lse_stride, long long n_vec,
-               int D, void* o_out, float* lse_out) {
+void launch_np(bool out_bf16, const MergeMap* map, unsigned blocks, cudaStream_t stream,
+               const float* o_parts, long long o_stride, const float* lse_parts,
+               long long lse_stride, long long n_vec, int D, void* o_out, float* lse_out) {
   constexpr int U = NP <= 4 ? 2 : 1;
+  if (map) {
+    long long rb = (map->row0[map->n_blocks] + 7) / 8;
+    if (rb > 152LL * 32) rb = 152LL * 32;
+    const unsigned nb = static_cast<unsigned>(std::max(1LL, rb));
+    if (out_bf16)
+      lse_merge_rows_kernel<NP, true><<<nb, 256, 0, stream>>>(o_parts, o_stride, lse_parts,
+                                                              lse_stride, D, o_out, lse_out, *map);
+    else
+      lse_merge_rows_kernel<NP, false><<<nb, 256, 0, stream>>>(o_parts, o_stride, lse_parts,
+                                                               lse_stride, D, o_out, lse_out, *map);
+    return;
+  }
   if (out_bf16)
     lse_merge_kernel<NP, true, U><<<blocks, 256, 0, stream>>>(o_parts, o_stride, lse_parts,
                                                               lse_stride, n_vec, D, o_out, lse_out);
@@ -110,7 +221,7 @@ void launch_np(bool out_bf16, unsigned blocks, cudaStream_t stream, const float*
 usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_stride,
                               const float* lse_parts, int64_t lse_part_stride, int64_t n_vec,
                               int D, void* o_out, bool out_bf16, float* lse_out,
-                              cudaStream_t stream) {
+                              const MergeMap* map, cudaStream_t stream) {
   if (n_vec == 0) return USP_OK;
   const long long total = n_vec * (D / 4);
   long long blocks = (total + 255) / 256;
@@ -118,8 +229,8 @@ usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_
   const unsigned nb = static_cast<unsigned>(blocks);
 #define USP_MERGE_CASE(N)                                                                        \
   case N:                                                                                        \
-    launch_np<N>(out_bf16, nb, stream, o_parts, o_part_stride, lse_parts, lse_part_stride, n_vec, \
-                 D, o_out, lse_out);                                                             \
+    launch_np<N>(out_bf16, map, nb, stream, o_parts, o_part_stride, lse_parts, lse_part_stride,    \
+                 n_vec, D, o_out, lse_out);                                                      \
     break;
   switch (n_parts) {
     USP_MERGE_CASE(1) USP_MERGE_CASE(2) USP_MERGE_CASE(3) USP_MERGE_CASE(4) USP_MERGE_CASE(5)
