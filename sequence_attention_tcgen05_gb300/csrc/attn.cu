@@ -2,7 +2,7 @@
 // 256-row query block) work unit, O = softmax(scale Q K^T + mask) V and its natural-log LSE
 // ([USP] the backend's (out, lse) for one ring step; [CP] Ring Attention).
 //
-// One persistent CTA per SM, three warpgroups (384 threads):
+// One persistent CTA per SM, five warpgroups (640 threads):
 //   WG0  warp 0: TMA producer — the unit's two 128-row Q tiles, then K and V tiles into a
 //                STAGES-deep ring (K and V of a key tile serve both query tiles).
 //        warp 1: MMA issuer (one thread) and TMEM owner.  Per key tile j, in this order:
@@ -10,18 +10,21 @@
 //                (SS MMA M=128 N=128 for the scores; TS MMA with P read from TMEM for P V), so the
 //                softmax of each query tile overlaps a score MMA and a P V MMA of the other tile.
 //        warps 2-3 idle.  The warpgroup gives registers away (setmaxnreg) to the softmax groups.
-//   WG1, WG2  softmax of query tile a / b: thread = query row = TMEM lane.  One 128-column
-//                tcgen05.ld of the S row, masking on boundary tiles, exp2 of
-//                s * scale log2e - m with packed fp32x2 fused multiply-adds, bf16 P written back
-//                over the first 64 columns of S, row sum in registers.  The running max m is raised
-//                only when a tile's max exceeds it by more than 8 (log2 units), and then O is
-//                rescaled in TMEM; otherwise the stale max stays, which bounds P by 2^8 and is
-//                exact after the final division by the row sum.  So once a row has a reference max
-//                the exponentials are computed against it straight away while the tile max is taken
-//                in the same pass (the exponentials are redone only when the max is raised).
-//                Epilogue: O / l to global memory (fp32 or bf16) and lse = (m + log2 l) ln 2.
-// TMEM (512 columns): S_a [0,128) S_b [128,256) O_a [256,256+D) O_b [256+D,256+2D); P_x aliases
-// the first 64 columns of S_x.  MMAs issued by one thread execute in issue order, so a completed
+//   WG1..WG4  softmax of query tile x = (wg-1)/2, key columns h*64..h*64+63 with h = (wg-1)%2:
+//                thread = query row = TMEM lane.  One 64-column tcgen05.ld of its half of the S row,
+//                masking on boundary tiles, partial row max, exchanged with the other half through
+//                shared memory (one mbarrier per tile), then 2^(s * scale log2e - m) with packed
+//                fp32x2 fused multiply-adds and MUFU ex2, bf16 P written over the first 32 columns
+//                of its own S half, partial row sum in registers.  The running max m is raised only
+//                when a tile's max exceeds it by more than 8 (log2 units); then each half rescales
+//                its half of O in TMEM.  Otherwise the stale max stays, which bounds P by 2^8 and
+//                is exact after the final division by the row sum.  Epilogue: the two partial
+//                row sums are combined, each half stores its half of O / l (fp32 or bf16) and the
+//                first half the lse = (m + log2 l) ln 2.
+// Splitting each tile's softmax over two warpgroups halves the softmax term of the chain
+// S_x(j) -> softmax -> O_x += P V -> S_x(j+1), which sets the kernel's period per key tile.
+// TMEM (512 columns): S_a [0,128) S_b [128,256) O_a [256,256+D) O_b [256+D,256+2D); P_x columns
+// [0,32) and [64,96) of S_x.  MMAs issued by one thread execute in issue order, so a completed
 // S_x(j) implies P V of tile j-1 of the same query tile has completed: S_x may then be read, P_x
 // rewritten and O_x rescaled without another wait.
 //
@@ -42,11 +45,13 @@ namespace {
 
 constexpr float kTau = 8.0f;  // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kThreads = 384;
-// Register split: 384 threads x 168 at launch = 64512 >= 128 x 80 (WG0) + 256 x 208 (softmax).
-constexpr uint32_t kRegsWG0 = 80;
-constexpr uint32_t kRegsSoftmax = 208;
-static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax <= kThreads * 168, "register split");
+constexpr int kThreads = 640;
+constexpr int kSoftmaxThreads = 256;  // the two warpgroups of one query tile
+// Register split: 640 threads x 96 at launch = 61440 >= 128 x 56 (WG0) + 512 x 104 (softmax).
+constexpr uint32_t kRegsLaunch = 96;
+constexpr uint32_t kRegsWG0 = 56;
+constexpr uint32_t kRegsSoftmax = 104;
+static_assert(128 * kRegsWG0 + 512 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 
 template <int D, int STAGES>
 struct Layout {
@@ -58,9 +63,11 @@ struct Layout {
   static constexpr int kV = kK + STAGES * kKBytes;
   static constexpr int kBar = kV + STAGES * kVBytes;
   // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2],
-  // o_empty[2], mma_done
-  static constexpr int kNumBars = 2 + 3 * STAGES + 9;
-  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  // o_empty[2], xch[2], xl[2], mma_done
+  static constexpr int kNumBars = 2 + 3 * STAGES + 13;
+  static constexpr int kXmax = kBar + kNumBars * 8;        // float [2 parity][2 tile][2 half][128]
+  static constexpr int kXsum = kXmax + 2 * 2 * 2 * 128 * 4;  // float [2 tile][2 half][128]
+  static constexpr int kTmemSlot = kXsum + 2 * 2 * 128 * 4;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
@@ -97,59 +104,45 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
   return u;
 }
 
-__device__ __forceinline__ float row_max(const uint32_t (&r)[kAttnBN]) {
-  float m8[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(r[i]);
-#pragma unroll
-  for (int i = 8; i < kAttnBN; i += 16)
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      m8[k] = fmax3(m8[k], __uint_as_float(r[i + 2 * k]), __uint_as_float(r[i + 2 * k + 1]));
-  return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-}
-
-// One pass over a 128-column score row: p = 2^(s * c + nb) for every column (MUFU ex2), written
-// as bf16 P over the first 64 TMEM columns at t_p; returns the fp32 row sum.  MAX: also returns
-// the raw row max in *mraw.
-template <bool MAX>
-__device__ __forceinline__ float exp_pass(const uint32_t (&r)[kAttnBN], uint64_t c2, float nb,
-                                          uint32_t t_p, float* mraw) {
+// 2^(s * c + nb) for the 64 columns of one half row: bf16 P written as 32 packed columns at t_p
+// (two 16-column stores); returns the fp32 sum.
+__device__ __forceinline__ float exp_half(const uint32_t (&r)[64], uint64_t c2, float nb,
+                                          uint32_t t_p) {
   const uint64_t nb2 = f2_pack(nb, nb);
-  uint64_t sum2[4];
+  uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) sum2[i] = 0ull;
-  float m8[8];
-  if (MAX) {
+  for (int chunk = 0; chunk < 2; ++chunk) {
+    uint32_t pk[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
-  }
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t pk[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int col = half * 64 + 2 * i;
-      const float s0 = __uint_as_float(r[col]), s1 = __uint_as_float(r[col + 1]);
-      if (MAX) m8[i & 7] = fmax3(m8[i & 7], s0, s1);
-      const uint64_t a2 = f2_fma(f2_pack(s0, s1), c2, nb2);
+    for (int i = 0; i < 16; ++i) {
+      const int col = chunk * 32 + 2 * i;
+      const uint64_t a2 =
+          f2_fma(f2_pack(__uint_as_float(r[col]), __uint_as_float(r[col + 1])), c2, nb2);
       float e0, e1;
       f2_unpack(a2, e0, e1);
       const float p0 = ex2_approx(e0);
       const float p1 = ex2_approx(e1);
-      sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
+      sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
       pk[i] = pack_bf16x2(p0, p1);
     }
-    tmem_st32(t_p + half * 32, pk);
+    tmem_st16(t_p + chunk * 16, pk);
   }
-  if (MAX)
-    *mraw = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-  float s0, s1, s2, s3, s4, s5, s6, s7;
+  float s0, s1, s2, s3;
   f2_unpack(sum2[0], s0, s1);
   f2_unpack(sum2[1], s2, s3);
-  f2_unpack(sum2[2], s4, s5);
-  f2_unpack(sum2[3], s6, s7);
-  return ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+  return (s0 + s1) + (s2 + s3);
+}
+
+__device__ __forceinline__ float half_max(const uint32_t (&r)[64]) {
+  float m8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(r[i]);
+#pragma unroll
+  for (int i = 8; i < 64; i += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      m8[k] = fmax3(m8[k], __uint_as_float(r[i + 2 * k]), __uint_as_float(r[i + 2 * k + 1]));
+  return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
 
 template <int D, int STAGES>
@@ -168,7 +161,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_empty = pv_done + 2;
-  uint64_t* mma_done = o_empty + 2;
+  uint64_t* xch = o_empty + 2;      // [2]: partial row max exchanged (per key tile)
+  uint64_t* xl = xch + 2;           // [2]: partial row sum exchanged (per unit)
+  uint64_t* mma_done = xl + 2;
+  float* xmax = reinterpret_cast<float*>(sm + L::kXmax);
+  float* xsum = reinterpret_cast<float*>(sm + L::kXsum);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbort);
   const int warp = threadIdx.x >> 5;
@@ -187,9 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], kSoftmaxThreads);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&o_empty[i], 128);
+      mbar_init(&o_empty[i], kSoftmaxThreads);
+      mbar_init(&xch[i], kSoftmaxThreads);
+      mbar_init(&xl[i], kSoftmaxThreads);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -255,20 +254,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint32_t q_base = smem_u32(sm + L::kQ);
       const uint32_t k_base = smem_u32(sm + L::kK);
       const uint32_t v_base = smem_u32(sm + L::kV);
+      static_assert(L::kAlloc < (1 << 18), "descriptor start addresses are 14-bit fields of addr >> 4");
       uint32_t stage = 0, phase = 0, q_iter = 0, units_done = 0;
       uint32_t gp[2] = {0, 0};  // P V count per query tile
       bool ok = true;
+      // Shared-memory descriptors (128-byte swizzle, SBO 1024 B, version 1): constant high word;
+      // low word = start address >> 4 | LBO field (1 for the K-major Q and K, 16384 B for V).
+      constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+      const uint32_t q_lo = (q_base >> 4) | (1u << 16);
+      const uint32_t k_lo = (k_base >> 4) | (1u << 16);
+      const uint32_t v_lo = (v_base >> 4) | ((static_cast<uint32_t>(kAttnBN * 128) >> 4) << 16);
       auto qk = [&](int x, uint32_t st) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qa = q_base + x * L::kQTile + (kk >> 2) * (kAttnBM * 128) + (kk & 3) * 32;
-          const uint32_t ka = k_base + st * L::kKBytes + (kk >> 2) * (kAttnBN * 128) + (kk & 3) * 32;
-          mma_ss(tmem + x * 128, sdesc_sw128(qa, 16, 1024), sdesc_sw128(ka, 16, 1024), idesc_qk,
-                 kk > 0 ? 1u : 0u);
-        }
+        const uint32_t a = q_lo + x * (L::kQTile >> 4);
+        const uint32_t b = k_lo + st * (L::kKBytes >> 4);
+        if (D == 128) mma_group_qk8(tmem + x * 128, a, b, kDescHi, idesc_qk);
+        else mma_group_qk4(tmem + x * 128, a, b, kDescHi, idesc_qk);
         mma_commit(&s_full[x]);
       };
-      // O_x += P_x V(st); `first` = first key tile of the unit (overwrites O_x)
+      // O_x += P_x V(st); `first` = first key tile of the unit (overwrites O_x).  P_x: keys 0-63
+      // packed in S_x columns [0,32), keys 64-127 in [64,96).
       auto pv = [&](int x, uint32_t st, uint32_t ph, bool first) -> bool {
         if (!mbar_wait(&p_full[x], gp[x] & 1, abort_flag, p.status, budget)) return false;
         if (first && units_done > 0 &&
@@ -276,12 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           return false;
         if (!mbar_wait(&v_full[st], ph, abort_flag, p.status, budget)) return false;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kAttnBN / 16; ++kk) {
-          const uint32_t va = v_base + st * L::kVBytes + kk * (16 * 128);
-          mma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8, sdesc_sw128(va, kAttnBN * 128, 1024),
-                 idesc_pv, (!first || kk > 0) ? 1u : 0u);
-        }
+        mma_group_pv(tmem + 256 + x * D, tmem + x * 128, v_lo + st * (L::kVBytes >> 4), kDescHi,
+                     idesc_pv, first ? 0u : 1u);
         mma_commit(&pv_done[x]);
         ++gp[x];
         return true;
@@ -320,15 +320,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else {
     // ------------------------------------------------------------------ softmax warpgroups
     regs_inc<kRegsSoftmax>();
-    const int x = wg - 1;  // query tile a (0) or b (1)
+    const int x = (wg - 1) >> 1;   // query tile a (0) or b (1)
+    const int hf = (wg - 1) & 1;   // key columns [hf*64, hf*64+64) of each tile
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t t_s = t_lane + x * 128;
-    const uint32_t t_o = t_lane + 256 + x * D;
+    const uint32_t t_s = t_lane + x * 128 + hf * 64;           // this half of S_x, and its P
+    const uint32_t t_o = t_lane + 256 + x * D + hf * (D / 2);  // this half of O_x
     const float c = p.scale_log2;  // > 0 (checked on the host)
     const uint64_t c2 = f2_pack(c, c);
-    uint32_t g = 0;
+    uint32_t g = 0, units = 0;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       const bool r = mbar_wait(bar, parity, abort_flag, p.status, budget);
@@ -344,73 +345,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                                  ? static_cast<long long>(s.o_start0) + static_cast<long long>(ol) * s.o_stride
                                  : static_cast<long long>(s.o_start1) + static_cast<long long>(ol - s.o_len0) * s.o_stride;
       const long long orow = static_cast<long long>(u.b) * s.o_bstride + opos;
-      const long long o_elem = (orow * s.o_heads + u.h) * D;
+      const long long o_elem = (orow * s.o_heads + u.h) * D + hf * (D / 2);
       if (u.n_kv == 0) {
         if (row_valid) {
           if (p.o_bf16) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.o) + o_elem);
-            for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+            for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
           } else {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(s.o) + o_elem);
-            for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < D / 8; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          if (s.lse) s.lse[orow * s.o_heads + u.h] = -INFINITY;
+          if (hf == 0 && s.lse) s.lse[orow * s.o_heads + u.h] = -INFINITY;
         }
         continue;
       }
       const int lim = s.diag == kNoDiag ? INT_MAX : q0 + row + s.diag;  // visible key c <= lim
-      float m_ref = -INFINITY;  // running max of scale*log2e*s, raised lazily
-      float l = 0.f;
+      float m_ref = -INFINITY;  // running max of scale*log2e*s, raised lazily (same in both halves)
+      float l = 0.f;            // row sum over this half's columns
       for (int j = 0; j < u.n_kv; ++j, ++g) {
         if (!wait_all(&s_full[x], g & 1)) { ok = false; break; }
         tc_fence_after();
-        uint32_t r[kAttnBN];
-        tmem_ld128(t_s, r);
+        uint32_t r[64];
+        tmem_ld64(t_s, r);
         tmem_wait_ld();
-        const int c0 = j * kAttnBN;
-        const bool need_mask = (c0 + kAttnBN > s.kv_len) ||
-                               (s.diag != kNoDiag && c0 + kAttnBN - 1 > q0 + s.diag);
+        const int c0 = j * kAttnBN + hf * 64;  // local key index of r[0]
+        const bool need_mask = (c0 + 64 > s.kv_len) || (s.diag != kNoDiag && c0 + 63 > q0 + s.diag);
         if (need_mask) {
-          const int last = min(s.kv_len - 1, lim) - c0;  // visible local columns: i <= last
+          const int last = min(s.kv_len - 1, lim) - c0;  // visible columns of this half: i <= last
 #pragma unroll
-          for (int i = 0; i < kAttnBN; ++i)
+          for (int i = 0; i < 64; ++i)
             if (i > last) r[i] = 0xff800000u;  // -inf
         }
+        // exchange the partial row max with the other half of the tile
+        const float pm = half_max(r);
+        float* xm = xmax + ((g & 1) * 4 + x * 2) * 128;
+        xm[hf * 128 + row] = pm;
+        mbar_arrive(&xch[x]);
+        if (!wait_all(&xch[x], g & 1)) { ok = false; break; }
+        const float mx = fmaxf(pm, xm[(1 - hf) * 128 + row]) * c;
         float alpha = 1.f;
         bool resc = false;
-        float sum;
-        if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
-          // no reference max yet in this warp: take the tile max first
-          const float mx = row_max(r) * c;
-          if (mx > m_ref + kTau) {
-            if (m_ref != -INFINITY) {
-              alpha = ex2_approx(m_ref - mx);
-              resc = true;
-            }
-            m_ref = mx;
+        if (mx > m_ref + kTau) {
+          if (m_ref != -INFINITY) {
+            alpha = ex2_approx(m_ref - mx);
+            resc = true;
           }
-          const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref;
-          sum = exp_pass<false>(r, c2, nb, t_s, nullptr);
-        } else {
-          // speculate: exponentiate against the running max while taking the tile max
-          float mraw;
-          sum = exp_pass<true>(r, c2, -m_ref, t_s, &mraw);
-          const float mx = mraw * c;
-          const bool raise = mx > m_ref + kTau;
-          if (__any_sync(0xffffffffu, raise)) {
-            if (raise) {
-              alpha = ex2_approx(m_ref - mx);
-              resc = true;
-              m_ref = mx;
-            }
-            sum = exp_pass<false>(r, c2, -m_ref, t_s, nullptr);
-          }
+          m_ref = mx;
         }
+        const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        const float sum = exp_half(r, c2, nb, t_s);
         l = l * alpha + sum;
         if (__any_sync(0xffffffffu, resc)) {
           // S_x(j) complete => P V of tile j-1 complete: O_x is stable
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < D / 64; ++cc) {
             uint32_t w[32];
             tmem_ld32(t_o + cc * 32, w);
             tmem_wait_ld();
@@ -424,42 +412,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         mbar_arrive(&p_full[x]);
       }
       if (!ok) break;
-      // epilogue: wait for the unit's last P V of this tile
+      // epilogue: combine the two partial row sums, then each half stores its half of O
+      float* xs = xsum + x * 2 * 128;
+      xs[hf * 128 + row] = l;
+      mbar_arrive(&xl[x]);
+      if (!wait_all(&xl[x], units & 1)) { ok = false; break; }
+      ++units;
+      const float lt = l + xs[(1 - hf) * 128 + row];
       if (!wait_all(&pv_done[x], (g - 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-      const float lse = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
+      const float inv_l = lt > 0.f ? 1.0f / lt : 0.f;
+      const float lse = lt > 0.f ? (m_ref + lg2_approx(lt)) * kLn2 : -INFINITY;
 #pragma unroll
-      for (int half = 0; half < D / 64; ++half) {
-        uint32_t o[64];
-        tmem_ld64(t_o + half * 64, o);
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(t_o + cc * 32, o);
         tmem_wait_ld();
-        if (half == D / 64 - 1) {
+        if (cc == D / 64 - 1) {
           tc_fence_before();
           mbar_arrive(&o_empty[x]);
         }
         if (row_valid) {
           if (p.o_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.o) + o_elem + half * 64);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.o) + o_elem + cc * 32);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(
                   pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
                   pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
                   pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
                   pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
           } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(s.o) + o_elem + half * 64);
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(s.o) + o_elem + cc * 32);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < 8; ++i)
               dst[i] = make_float4(__uint_as_float(o[4 * i + 0]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
                                    __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
           }
         }
       }
-      if (row_valid) {
-        if (s.lse) s.lse[orow * s.o_heads + u.h] = lse;
-      }
+      if (row_valid && hf == 0 && s.lse) s.lse[orow * s.o_heads + u.h] = lse;
     }
   }
 

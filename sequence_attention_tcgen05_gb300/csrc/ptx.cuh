@@ -156,6 +156,32 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// S = A B^T over K = 128 (the 8 K-steps of a 128x128 score tile), issued as one block:
+// a_lo / b_lo are the low descriptor words of the K-step-0 operands (start address >> 4 | LBO field),
+// hi the shared high word; K-step kk adds (kk / 4) * 1024 + (kk % 4) * 2 (16-byte units) to both.
+__device__ __forceinline__ void mma_group_qk8(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                              uint32_t hi, uint32_t idesc) {
+  asm volatile("{\n\t.reg .pred pz, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 pz, 0, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pz;\n\tadd.u32 alo, %1, 2;\n\tadd.u32 blo, %2, 2;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 4;\n\tadd.u32 blo, %2, 4;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 6;\n\tadd.u32 blo, %2, 6;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1024;\n\tadd.u32 blo, %2, 1024;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1026;\n\tadd.u32 blo, %2, 1026;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1028;\n\tadd.u32 blo, %2, 1028;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1030;\n\tadd.u32 blo, %2, 1030;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc) : "memory");
+}
+
+// S = A B^T over K = 64 (the 4 K-steps of a 128x128 score tile), issued as one block:
+// a_lo / b_lo are the low descriptor words of the K-step-0 operands (start address >> 4 | LBO field),
+// hi the shared high word; K-step kk adds (kk / 4) * 1024 + (kk % 4) * 2 (16-byte units) to both.
+__device__ __forceinline__ void mma_group_qk4(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                              uint32_t hi, uint32_t idesc) {
+  asm volatile("{\n\t.reg .pred pz, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 pz, 0, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pz;\n\tadd.u32 alo, %1, 2;\n\tadd.u32 blo, %2, 2;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 4;\n\tadd.u32 blo, %2, 4;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 6;\n\tadd.u32 blo, %2, 6;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc) : "memory");
+}
+
+// O (+)= P V over the 128 keys of a tile, issued as one block: P from TMEM (keys 0-63 at columns
+// p_tmem + [0, 32), keys 64-127 at p_tmem + [64, 96)), V from shared memory (MN-major, K-step kk
+// adds kk * 128 in 16-byte units to b_lo); the first K-step accumulates iff acc_first != 0.
+__device__ __forceinline__ void mma_group_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t b_lo,
+                                             uint32_t hi, uint32_t idesc, uint32_t acc_first) {
+  asm volatile("{\n\t.reg .pred pf, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 db;\n\tsetp.ne.b32 pf, %5, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pf;\n\tadd.u32 alo, %1, 8;\n\tadd.u32 blo, %2, 128;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 16;\n\tadd.u32 blo, %2, 256;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 24;\n\tadd.u32 blo, %2, 384;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 64;\n\tadd.u32 blo, %2, 512;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 72;\n\tadd.u32 blo, %2, 640;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 80;\n\tadd.u32 blo, %2, 768;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 88;\n\tadd.u32 blo, %2, 896;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(p_tmem), "r"(b_lo), "r"(hi), "r"(idesc),
+               "r"(acc_first)
+               : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -197,6 +223,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 
