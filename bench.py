@@ -44,8 +44,8 @@ NOMINAL_HBM_GBS = 8000.0
 # DRAM bytes (read + write) per launch of the partial-attention kernel from an ncu capture, with
 # the hash of the kernel sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.105920 MB + write 3.704064 MB
-    "flux_1024_u2": {"bytes": 88809984, "kernel_hash": "3f4ac5271d81dc87"},
+    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.089536 MB + write 3.864320 MB
+    "flux_1024_u2": {"bytes": 88953856, "kernel_hash": "0c426f06c75cdad9"},
 }
 
 
