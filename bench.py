@@ -5,7 +5,12 @@ One step = one usp_attention call on the workload (fused reorder + seq->head re-
 the partial-attention launch over every chunk pair; the LSE merge of ring partials; the fused
 head->seq re-layout of O and LSE).  Inputs are resident in HBM when the timed region starts; the
 L2 cache is flushed between steps (outside the step's events) because the inputs of the default
-workload fit in L2.  Times come from CUDA events on the launching stream.
+workload fit in L2.  The flush READS a 256 MiB buffer: a flush that writes would leave up to the
+whole L2 dirty, and writing those lines back would then be charged to the timed kernels.  Each
+step is bracketed by one pair of events; a short spin kernel after the flush lets the host enqueue
+the step before the GPU reaches the start event, so the step's time is device execution (host
+planning and launch latency are in the e2e figure).  The per-phase breakdown comes from a second
+loop whose events sit between the phases.  Times come from CUDA events on the launching stream.
 
   value     attention TFLOP/s of the whole step: algorithmic FLOPs 4 B H D x (visible query/key
             pairs) over the step's device time (all phases), summed over ranks.
@@ -44,8 +49,8 @@ NOMINAL_HBM_GBS = 8000.0
 # DRAM bytes (read + write) per launch of the partial-attention kernel from an ncu capture, with
 # the hash of the kernel sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.089536 MB + write 3.864320 MB
-    "flux_1024_u2": {"bytes": 88953856, "kernel_hash": "0c426f06c75cdad9"},
+    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.084160 MB + write 3.922688 MB
+    "flux_1024_u2": {"bytes": 89006848, "kernel_hash": "0c426f06c75cdad9"},
 }
 
 
@@ -202,6 +207,28 @@ def phase_bytes(w, out_elem: int):
     return b
 
 
+def gpu_head_start(us: float = 60.0):
+    """Keeps the GPU busy for about ``us`` microseconds (a spin kernel) so that the host can enqueue
+    the next timed region before the GPU reaches its start event: the region then measures device
+    execution, not host launch latency (which the e2e figure includes)."""
+    import torch
+    torch.cuda._sleep(int(us * 2000))
+
+
+class L2Flush:
+    """Evicts the L2 cache (129 MB) by reading a 256 MiB buffer; the lines it leaves are clean, so
+    no write-back of earlier data falls into the next timed region."""
+
+    def __init__(self, device):
+        import torch
+        self.buf = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=device)
+        self.acc = torch.zeros((), dtype=torch.float32, device=device)
+
+    def __call__(self):
+        import torch
+        torch.sum(self.buf, 0, out=self.acc)
+
+
 def standalone_relayout(w, q, k, v, o, flush, stream, reps: int = 50):
     """GB/s of the standalone Ulysses re-layout entry points on this workload's tensors: seq->head
     of Q, K, V and head->seq of O over the Ulysses split (a separately timed measurement, since the
@@ -216,7 +243,8 @@ def standalone_relayout(w, q, k, v, o, flush, stream, reps: int = 50):
     e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
     t_in = t_out = 0.0
     for i in range(reps + 3):
-        flush.zero_()
+        flush()
+        gpu_head_start(300.0)
         e0.record(stream)
         for x, y in zip((q, k, v), outs):
             usp.usp_relayout_seq2head(x, y, w.B, w.H, w.D, lens, stream=stream)
@@ -308,7 +336,7 @@ def config_of(w, out_dtype: str):
             "ulysses_degree": w.ulysses_degree, "ring_degree": w.ring_degree,
             "causal": w.causal, "order": w.order, "text_rows": w.text_rows,
             "seq_lens": list(w.seq_lens) or "default split", "out_dtype": out_dtype,
-            "l2": "flushed between timed steps (256 MiB write outside the step events)"}
+            "l2": "flushed between timed steps (256 MiB read outside the step events)"}
 
 
 def run_ours(args):
@@ -339,7 +367,7 @@ def run_ours(args):
     nbytes = usp.usp_attention_workspace_size(B, S, H, D, w.ulysses_degree, w.ring_degree,
                                               w.order, o_code)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)  # 256 MiB > L2
+    flush = L2Flush(device)  # 256 MiB > L2
     stream = torch.cuda.current_stream()
     seq = list(w.seq_lens) or None
 
@@ -352,41 +380,54 @@ def run_ours(args):
     events = make_events()
     handles = [e.cuda_event for e in events]
 
-    def step():
+    def step(evs):
         return usp.usp_attention_events(q, k, v, B, S, H, D, scale, w.causal, w.ulysses_degree,
-                                        w.ring_degree, o, lse, ws, nbytes, handles, seq, None,
+                                        w.ring_degree, o, lse, ws, nbytes, evs, seq, None,
                                         w.order, o_code, stream)
 
+    no_events = [None] * 5
     for _ in range(args.warmup):
-        flush.zero_()
-        step()
+        flush()
+        step(handles)
     torch.cuda.synchronize()
     if usp.usp_check_status(ws) != usp.USP_OK:
         raise RuntimeError("device status after warm-up: " + usp.lib().usp_last_error().decode())
 
+    # headline: one event pair around each step; the flush and a short GPU spin before the start
+    # event let the host enqueue the whole step before the GPU reaches it
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    phases = {"qkv_relayout": 0.0, "attention": 0.0, "merge": 0.0, "out_relayout": 0.0}
+    e_begin, e_finish = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     total_ms = 0.0
     launches = 0
     barrier(device)
     torch.cuda.synchronize()
     clocks.mark()
     for _ in range(args.steps):
-        flush.zero_()
-        launches += step()
-        events[4].synchronize()
-        t = [events[i].elapsed_time(events[i + 1]) for i in range(4)]
-        phases["qkv_relayout"] += t[0]
-        phases["attention"] += t[1]
-        phases["merge"] += t[2]
-        phases["out_relayout"] += t[3]
-        total_ms += sum(t)
+        flush()
+        gpu_head_start()
+        e_begin.record(stream)
+        launches += step(no_events)
+        e_finish.record(stream)
+        e_finish.synchronize()
+        total_ms += e_begin.elapsed_time(e_finish)
     torch.cuda.synchronize()
     barrier(device)
     clocks.mark()
     clk = clocks.stop()
+
+    # per-phase breakdown (separate loop: the phase events themselves cost about 2 us each)
+    phases = {"qkv_relayout": 0.0, "attention": 0.0, "merge": 0.0, "out_relayout": 0.0}
+    breakdown_steps = min(args.steps, 200)
+    for _ in range(breakdown_steps):
+        flush()
+        gpu_head_start()
+        step(handles)
+        events[4].synchronize()
+        t = [events[i].elapsed_time(events[i + 1]) for i in range(4)]
+        for name, dt in zip(phases, t):
+            phases[name] += dt
     status = usp.usp_check_status(ws)
     if status != usp.USP_OK:
         raise RuntimeError("device status after timing: " + usp.lib().usp_last_error().decode())
@@ -400,7 +441,7 @@ def run_ours(args):
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
     for i in range(e2e_steps + 1):
-        flush.zero_()
+        flush()
         e_start.record(stream)
         for dst, src in zip((q, k, v), host):
             dst.copy_(src, non_blocking=True)
@@ -417,7 +458,7 @@ def run_ours(args):
     d2h = B * S * H * D * out_elem + B * S * H * 4
 
     peaks, peak_kind = load_peaks()
-    att_s = phases["attention"] / 1000.0 / args.steps
+    att_s = phases["attention"] / 1000.0 / breakdown_steps
     achieved = flops / att_s / 1e12
     peak = peaks["bf16_tflops"]
     traffic = ATTN_TRAFFIC.get(w.name)
@@ -426,7 +467,7 @@ def run_ours(args):
     bw = {}
     for name in ("qkv_relayout", "merge"):
         if pb[name]:
-            s = phases[name] / 1000.0 / args.steps
+            s = phases[name] / 1000.0 / breakdown_steps
             gbs = pb[name] / s / 1e9
             bw[name] = {"GB/s": gbs, "bytes": pb[name], "us": s * 1e6,
                         "frac_measured_hbm": gbs / peaks["hbm_gbs"], "frac_8TBs": gbs / NOMINAL_HBM_GBS}
@@ -435,7 +476,7 @@ def run_ours(args):
     for part in ("seq2head_qkv", "head2seq_o"):
         standalone[part]["frac_measured_hbm"] = standalone[part]["GB/s"] / peaks["hbm_gbs"]
         standalone[part]["frac_8TBs"] = standalone[part]["GB/s"] / NOMINAL_HBM_GBS
-    bw_s = sum(phases[n] for n in ("qkv_relayout", "merge")) / 1000.0 / args.steps
+    bw_s = sum(phases[n] for n in ("qkv_relayout", "merge")) / 1000.0 / breakdown_steps
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -451,7 +492,8 @@ def run_ours(args):
                            "frac_measured_hbm": (bw_bytes / bw_s / 1e9 / peaks["hbm_gbs"]) if bw_s > 0 else None,
                            "frac_8TBs": (bw_bytes / bw_s / 1e9 / NOMINAL_HBM_GBS) if bw_s > 0 else None,
                            "phases": bw, "standalone_relayout": standalone},
-        "phases_ms_per_step": {k: v / args.steps for k, v in phases.items()},
+        "phases_ms_per_step": {k: v / breakdown_steps for k, v in phases.items()},
+        "phases_steps": breakdown_steps,
         "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
