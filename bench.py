@@ -50,6 +50,7 @@ NOMINAL_HBM_GBS = 8000.0
 # the hash of the kernel sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
     # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.084160 MB + write 3.922688 MB
+    # (taken on the kernel before the K/V barrier merge; null until re-captured)
     "flux_1024_u2": {"bytes": 89006848, "kernel_hash": "0c426f06c75cdad9"},
 }
 

@@ -62,9 +62,9 @@ struct Layout {
   static constexpr int kK = kQ + 2 * kQTile;
   static constexpr int kV = kK + STAGES * kKBytes;
   static constexpr int kBar = kV + STAGES * kVBytes;
-  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2],
+  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2],
   // o_empty[2], xch[2], xl[2], mma_done
-  static constexpr int kNumBars = 2 + 3 * STAGES + 13;
+  static constexpr int kNumBars = 2 + 2 * STAGES + 13;
   static constexpr int kXmax = kBar + kNumBars * 8;        // float [2 parity][2 tile][2 half][128]
   static constexpr int kXsum = kXmax + 2 * 2 * 2 * 128 * 4;  // float [2 tile][2 half][128]
   static constexpr int kTmemSlot = kXsum + 2 * 2 * 128 * 4;
@@ -154,9 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* v_full = k_full + STAGES;
-  uint64_t* kv_empty = v_full + STAGES;
+  uint64_t* kv_full = bars + 2;  // K and V of a stage, one transaction count
+  uint64_t* kv_empty = kv_full + STAGES;
   uint64_t* s_full = kv_empty + STAGES;  // [2]: query tile a, b
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
@@ -178,8 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -225,16 +223,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         bool ok = true;
         for (int j = 0; j < u.n_kv; ++j) {
           if (!mbar_wait(&kv_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
-          mbar_arrive_expect_tx(&k_full[stage], L::kKBytes);
+          mbar_arrive_expect_tx(&kv_full[stage], L::kKBytes + L::kVBytes);
 #pragma unroll
           for (int blk = 0; blk < D / 64; ++blk)
             tma_load_4d(sm + L::kK + stage * L::kKBytes + blk * kAttnBN * 128, &p.maps[s.k_map],
-                        blk * 64, u.h, kvrow + j * kAttnBN, u.b, &k_full[stage]);
-          mbar_arrive_expect_tx(&v_full[stage], L::kVBytes);
+                        blk * 64, u.h, kvrow + j * kAttnBN, u.b, &kv_full[stage]);
 #pragma unroll
           for (int blk = 0; blk < D / 64; ++blk)
             tma_load_4d(sm + L::kV + stage * L::kVBytes + blk * kAttnBN * 128, &p.maps[s.v_map],
-                        blk * 64, u.h, kvrow + j * kAttnBN, u.b, &v_full[stage]);
+                        blk * 64, u.h, kvrow + j * kAttnBN, u.b, &kv_full[stage]);
           ++fills[stage];
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -242,8 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       for (int s = 0; s < STAGES; ++s) {
         if (fills[s]) {
-          mbar_drain(&k_full[s], (fills[s] - 1) & 1, drain_budget);
-          mbar_drain(&v_full[s], (fills[s] - 1) & 1, drain_budget);
+          mbar_drain(&kv_full[s], (fills[s] - 1) & 1, drain_budget);
         }
       }
       if (q_iter) mbar_drain(q_full, (q_iter - 1) & 1, drain_budget);
@@ -271,45 +267,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         else mma_group_qk4(tmem + x * 128, a, b, kDescHi, idesc_qk);
         mma_commit(&s_full[x]);
       };
-      // O_x += P_x V(st); `first` = first key tile of the unit (overwrites O_x).  P_x: keys 0-63
-      // packed in S_x columns [0,32), keys 64-127 in [64,96).
-      auto pv = [&](int x, uint32_t st, uint32_t ph, bool first) -> bool {
+      // O_x += P_x V(st); `first` = first key tile of the unit (overwrites O_x), `last` = its last
+      // one (pv_done tells the epilogue that O_x is final).  P_x: keys 0-63 packed in S_x columns
+      // [0,32), keys 64-127 in [64,96).  V(st) arrived with K(st): the S MMA of this stage waited.
+      auto pv = [&](int x, uint32_t st, bool first, bool last) -> bool {
         if (!mbar_wait(&p_full[x], gp[x] & 1, abort_flag, p.status, budget)) return false;
         if (first && units_done > 0 &&
             !mbar_wait(&o_empty[x], (units_done - 1) & 1, abort_flag, p.status, budget))
           return false;
-        if (!mbar_wait(&v_full[st], ph, abort_flag, p.status, budget)) return false;
         tc_fence_after();
         mma_group_pv(tmem + 256 + x * D, tmem + x * 128, v_lo + st * (L::kVBytes >> 4), kDescHi,
                      idesc_pv, first ? 0u : 1u);
-        mma_commit(&pv_done[x]);
+        if (last) mma_commit(&pv_done[x]);
         ++gp[x];
         return true;
       };
       for (int unit = blockIdx.x; unit < p.n_units && ok; unit += gridDim.x) {
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
+        // Q and K/V come from TMA (async proxy, like the MMAs): the barrier waits order them, no
+        // tcgen05 fence is needed; P comes from tcgen05.st of other threads (fence in pv()).
         if (!mbar_wait(q_full, q_iter & 1, abort_flag, p.status, budget)) break;
         ++q_iter;
-        tc_fence_after();
-        uint32_t prev_stage = 0, prev_phase = 0;
+        uint32_t prev_stage = 0;
         for (int j = 0; j < u.n_kv; ++j) {
-          if (!mbar_wait(&k_full[stage], phase, abort_flag, p.status, budget)) { ok = false; break; }
-          tc_fence_after();
+          if (!mbar_wait(&kv_full[stage], phase, abort_flag, p.status, budget)) { ok = false; break; }
           qk(0, stage);
           if (j > 0) {
-            if (!pv(1, prev_stage, prev_phase, j == 1)) { ok = false; break; }
+            if (!pv(1, prev_stage, j == 1, false)) { ok = false; break; }
             mma_commit(&kv_empty[prev_stage]);
           }
           qk(1, stage);
           if (j == u.n_kv - 1) mma_commit(q_empty);
-          if (!pv(0, stage, phase, j == 0)) { ok = false; break; }
+          if (!pv(0, stage, j == 0, j == u.n_kv - 1)) { ok = false; break; }
           prev_stage = stage;
-          prev_phase = phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        if (!pv(1, prev_stage, prev_phase, u.n_kv == 1)) { ok = false; break; }
+        if (!pv(1, prev_stage, u.n_kv == 1, true)) { ok = false; break; }
         mma_commit(&kv_empty[prev_stage]);
         ++units_done;
       }
@@ -417,9 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       xs[hf * 128 + row] = l;
       mbar_arrive(&xl[x]);
       if (!wait_all(&xl[x], units & 1)) { ok = false; break; }
-      ++units;
       const float lt = l + xs[(1 - hf) * 128 + row];
-      if (!wait_all(&pv_done[x], (g - 1) & 1)) { ok = false; break; }
+      if (!wait_all(&pv_done[x], units & 1)) { ok = false; break; }  // committed once per unit
+      ++units;
       tc_fence_after();
       const float inv_l = lt > 0.f ? 1.0f / lt : 0.f;
       const float lse = lt > 0.f ? (m_ref + lg2_approx(lt)) * kLn2 : -INFINITY;
