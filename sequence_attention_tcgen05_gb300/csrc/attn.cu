@@ -10,21 +10,24 @@
 //                (SS MMA M=128 N=128 for the scores; TS MMA with P read from TMEM for P V), so the
 //                softmax of each query tile overlaps a score MMA and a P V MMA of the other tile.
 //        warps 2-3 idle.  The warpgroup gives registers away (setmaxnreg) to the softmax groups.
-//   WG1..WG4  softmax of query tile x = (wg-1)/2, key columns h*64..h*64+63 with h = (wg-1)%2:
-//                thread = query row = TMEM lane.  One 64-column tcgen05.ld of its half of the S row,
-//                masking on boundary tiles, partial row max, exchanged with the other half through
-//                shared memory (one mbarrier per tile), then 2^(s * scale log2e - m) with packed
-//                fp32x2 fused multiply-adds and MUFU ex2, bf16 P written over the first 32 columns
-//                of its own S half, partial row sum in registers.  The running max m is raised only
-//                when a tile's max exceeds it by more than 8 (log2 units); then each half rescales
-//                its half of O in TMEM.  Otherwise the stale max stays, which bounds P by 2^8 and
-//                is exact after the final division by the row sum.  Epilogue: the two partial
-//                row sums are combined, each half stores its half of O / l (fp32 or bf16) and the
-//                first half the lse = (m + log2 l) ln 2.
-// Splitting each tile's softmax over two warpgroups halves the softmax term of the chain
-// S_x(j) -> softmax -> O_x += P V -> S_x(j+1), which sets the kernel's period per key tile.
-// TMEM (512 columns): S_a [0,128) S_b [128,256) O_a [256,256+D) O_b [256+D,256+2D); P_x columns
-// [0,32) and [64,96) of S_x.  MMAs issued by one thread execute in issue order, so a completed
+//   WG1..WG4  softmax of query tile x = (wg-1)/2 over lane half h = (wg-1)%2 of every 32-lane TMEM
+//                quadrant: each thread owns two rows of the tile (quadrant lanes 16h + t/4 and that
+//                + 8) and a quarter of their 128 key columns (8k + 2(t%4) + {0,1}), read with one
+//                16-lane tcgen05.ld (.16x256b.x16).  Row maxima and sums combine over the four
+//                threads of a row with two warp shuffles, so the two warpgroups of a tile never
+//                wait for each other.  Masking on boundary tiles, 2^(s * scale log2e - m) with packed
+//                fp32x2 fused multiply-adds and MUFU ex2; each thread's column pair becomes one
+//                bf16x2 P word that a .16x128b tcgen05.st puts exactly at P column 4k + t%4, so P
+//                for the tile's 128 keys is packed over S_x columns [0, 64).  The running max m is
+//                raised only when a tile's max exceeds it by more than 8 (log2 units); then the
+//                thread rescales its part of O in TMEM.  Otherwise the stale max stays, which bounds
+//                P by 2^8 and is exact after the final division by the row sum.  Epilogue: O / l
+//                (fp32 or bf16) and lse = (m + log2 l) ln 2 stored from the same fragments.
+// Without a max exchange between the warpgroups the softmax term of the chain
+// S_x(j) -> softmax -> O_x += P V -> S_x(j+1), which sets the kernel's period per key tile, is
+// one warpgroup's own work.
+// TMEM (512 columns): S_a [0,128) S_b [128,256) O_a [256,256+D) O_b [256+D,256+2D); P_x packed in
+// columns [0,64) of S_x.  MMAs issued by one thread execute in issue order, so a completed
 // S_x(j) implies P V of tile j-1 of the same query tile has completed: S_x may then be read, P_x
 // rewritten and O_x rescaled without another wait.
 //
@@ -62,12 +65,10 @@ struct Layout {
   static constexpr int kK = kQ + 2 * kQTile;
   static constexpr int kV = kK + STAGES * kKBytes;
   static constexpr int kBar = kV + STAGES * kVBytes;
-  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2],
-  // o_empty[2], xch[2], xl[2], mma_done
-  static constexpr int kNumBars = 2 + 2 * STAGES + 13;
-  static constexpr int kXmax = kBar + kNumBars * 8;        // float [2 parity][2 tile][2 half][128]
-  static constexpr int kXsum = kXmax + 2 * 2 * 2 * 128 * 4;  // float [2 tile][2 half][128]
-  static constexpr int kTmemSlot = kXsum + 2 * 2 * 128 * 4;
+  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2], o_empty[2],
+  // mma_done
+  static constexpr int kNumBars = 2 + 2 * STAGES + 9;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
@@ -104,45 +105,54 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
   return u;
 }
 
-// 2^(s * c + nb) for the 64 columns of one half row: bf16 P written as 32 packed columns at t_p
-// (two 16-column stores); returns the fp32 sum.
-__device__ __forceinline__ float exp_half(const uint32_t (&r)[64], uint64_t c2, float nb,
-                                          uint32_t t_p) {
-  const uint64_t nb2 = f2_pack(nb, nb);
-  uint64_t sum2[2] = {0ull, 0ull};
-#pragma unroll
-  for (int chunk = 0; chunk < 2; ++chunk) {
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int col = chunk * 32 + 2 * i;
-      const uint64_t a2 =
-          f2_fma(f2_pack(__uint_as_float(r[col]), __uint_as_float(r[col + 1])), c2, nb2);
-      float e0, e1;
-      f2_unpack(a2, e0, e1);
-      const float p0 = ex2_approx(e0);
-      const float p1 = ex2_approx(e1);
-      sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
-      pk[i] = pack_bf16x2(p0, p1);
-    }
-    tmem_st16(t_p + chunk * 16, pk);
-  }
-  float s0, s1, s2, s3;
-  f2_unpack(sum2[0], s0, s1);
-  f2_unpack(sum2[1], s2, s3);
-  return (s0 + s1) + (s2 + s3);
-}
-
-__device__ __forceinline__ float half_max(const uint32_t (&r)[64]) {
+// Max over one row's 32 values of a 16x256b.x16 load (registers 4k + 2i + {0,1}, k < 16), then
+// over the four threads that share the row.
+__device__ __forceinline__ float row_max4(const uint32_t (&r)[64], int i) {
   float m8[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(r[i]);
+  for (int k = 0; k < 8; ++k)
+    m8[k] = fmax3(__uint_as_float(r[4 * k + 2 * i]), __uint_as_float(r[4 * k + 2 * i + 1]),
+                  __uint_as_float(r[4 * (k + 8) + 2 * i]));
 #pragma unroll
-  for (int i = 8; i < 64; i += 16)
+  for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], __uint_as_float(r[4 * (k + 8) + 2 * i + 1]));
+  float m = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  return fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+}
+
+// P = 2^(s * c + nb_i) for the thread's 64 values (row i uses nb_i), as bf16 pairs: the pair of
+// columns 8k + 2(t%4) + {0,1} (registers 4k + 2i + {0,1}, adjacent, so each packed fp32x2 op
+// reads a register pair as it is) is P column 4k + t%4, which is where a 16x128b store puts
+// register 2k + i.  Two stores of 32 P columns; returns the fp32 row sums of the unrounded values.
+__device__ __forceinline__ void exp_tile(const uint32_t (&r)[64], uint64_t c2, float nb0, float nb1,
+                                         uint32_t t_p, float (&sum)[2]) {
+  const uint64_t nbr[2] = {f2_pack(nb0, nb0), f2_pack(nb1, nb1)};
+  uint64_t acc[2] = {0ull, 0ull};  // row 0, row 1
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      m8[k] = fmax3(m8[k], __uint_as_float(r[i + 2 * k]), __uint_as_float(r[i + 2 * k + 1]));
-  return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+  for (int half = 0; half < 2; ++half) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int k = half * 8 + kk;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint64_t a2 = f2_fma(f2_pack(__uint_as_float(r[4 * k + 2 * i]), __uint_as_float(r[4 * k + 2 * i + 1])),
+                                   c2, nbr[i]);
+        float e0, e1;
+        f2_unpack(a2, e0, e1);
+        const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+        acc[i] = f2_add(acc[i], f2_pack(p0, p1));
+        pk[2 * kk + i] = pack_bf16x2(p0, p1);
+      }
+    }
+    tmem_st_16x128b_x8(t_p + half * 32, pk);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    float s0, s1;
+    f2_unpack(acc[i], s0, s1);
+    sum[i] = s0 + s1;
+  }
 }
 
 template <int D, int STAGES>
@@ -160,11 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_empty = pv_done + 2;
-  uint64_t* xch = o_empty + 2;      // [2]: partial row max exchanged (per key tile)
-  uint64_t* xl = xch + 2;           // [2]: partial row sum exchanged (per unit)
-  uint64_t* mma_done = xl + 2;
-  float* xmax = reinterpret_cast<float*>(sm + L::kXmax);
-  float* xsum = reinterpret_cast<float*>(sm + L::kXsum);
+  uint64_t* mma_done = o_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbort);
   const int warp = threadIdx.x >> 5;
@@ -185,8 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(&p_full[i], kSoftmaxThreads);
       mbar_init(&pv_done[i], 1);
       mbar_init(&o_empty[i], kSoftmaxThreads);
-      mbar_init(&xch[i], kSoftmaxThreads);
-      mbar_init(&xl[i], kSoftmaxThreads);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -314,14 +318,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
   } else {
     // ------------------------------------------------------------------ softmax warpgroups
+    // Warpgroup wg (1..4) serves query tile x = (wg-1)/2 and, within every 32-lane quadrant of
+    // TMEM, lane half hl = (wg-1)%2 (lanes 16*hl .. 16*hl+15 of the quadrant).  A thread owns
+    // two rows, lanes q*32 + 16*hl + lane/4 and that + 8, and one quarter of their columns:
+    // 16-lane loads give it columns 8k + 2(lane%4) + {0,1}; the four threads of a row combine
+    // their maxima and sums with two shuffles.
     regs_inc<kRegsSoftmax>();
     const int x = (wg - 1) >> 1;   // query tile a (0) or b (1)
-    const int hf = (wg - 1) & 1;   // key columns [hf*64, hf*64+64) of each tile
+    const int hl = (wg - 1) & 1;   // lane half of each quadrant
     const int wq = warp & 3;
-    const int row = wq * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t t_s = t_lane + x * 128 + hf * 64;           // this half of S_x, and its P
-    const uint32_t t_o = t_lane + 256 + x * D + hf * (D / 2);  // this half of O_x
+    const int lane_base = wq * 32 + hl * 16;
+    const int rw[2] = {lane_base + (lane >> 2), lane_base + (lane >> 2) + 8};  // tile rows
+    const int cq = 2 * (lane & 3);  // first of this thread's two columns in every 8-column group
+    const uint32_t t_base = tmem + (static_cast<uint32_t>(lane_base) << 16);
+    const uint32_t t_s = t_base + x * 128;  // S_x; P_x packed over its columns [0, 64)
+    const uint32_t t_o = t_base + 256 + x * D;
     const float c = p.scale_log2;  // > 0 (checked on the host)
     const uint64_t c2 = f2_pack(c, c);
     uint32_t g = 0, units = 0;
@@ -334,72 +345,89 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const Unit u = decode_unit(p, unit);
       const AttnSeg& s = *u.seg;
       const int q0 = u.q0 + x * kAttnBM;  // first local row of this query tile
-      const bool row_valid = row < u.qv[x];
-      const int ol = s.o_row0 + q0 + row;  // output-side local row
-      const long long opos = ol < s.o_len0
-                                 ? static_cast<long long>(s.o_start0) + static_cast<long long>(ol) * s.o_stride
-                                 : static_cast<long long>(s.o_start1) + static_cast<long long>(ol - s.o_len0) * s.o_stride;
-      const long long orow = static_cast<long long>(u.b) * s.o_bstride + opos;
-      const long long o_elem = (orow * s.o_heads + u.h) * D + hf * (D / 2);
+      bool row_valid[2];
+      long long o_elem[2], lse_at[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        row_valid[i] = rw[i] < u.qv[x];
+        const int ol = s.o_row0 + q0 + rw[i];  // output-side local row
+        const long long opos = ol < s.o_len0
+                                   ? static_cast<long long>(s.o_start0) + static_cast<long long>(ol) * s.o_stride
+                                   : static_cast<long long>(s.o_start1) + static_cast<long long>(ol - s.o_len0) * s.o_stride;
+        const long long orow = static_cast<long long>(u.b) * s.o_bstride + opos;
+        o_elem[i] = (orow * s.o_heads + u.h) * D;
+        lse_at[i] = orow * s.o_heads + u.h;
+      }
       if (u.n_kv == 0) {
-        if (row_valid) {
-          if (p.o_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.o) + o_elem);
-            for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(s.o) + o_elem);
-            for (int i = 0; i < D / 8; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (!row_valid[i]) continue;
+          for (int k = 0; k < D / 8; ++k) {
+            if (p.o_bf16) {
+              reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(s.o) + o_elem[i] + 8 * k + cq)[0] = 0u;
+            } else {
+              reinterpret_cast<float2*>(static_cast<float*>(s.o) + o_elem[i] + 8 * k + cq)[0] = make_float2(0.f, 0.f);
+            }
           }
-          if (hf == 0 && s.lse) s.lse[orow * s.o_heads + u.h] = -INFINITY;
+          if ((lane & 3) == 0 && s.lse) s.lse[lse_at[i]] = -INFINITY;
         }
         continue;
       }
-      const int lim = s.diag == kNoDiag ? INT_MAX : q0 + row + s.diag;  // visible key c <= lim
-      float m_ref = -INFINITY;  // running max of scale*log2e*s, raised lazily (same in both halves)
-      float l = 0.f;            // row sum over this half's columns
+      int lim[2];  // visible key c <= lim (local key index)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) lim[i] = s.diag == kNoDiag ? INT_MAX : q0 + rw[i] + s.diag;
+      float m_ref[2] = {-INFINITY, -INFINITY};  // running max of scale*log2e*s, raised lazily
+      float l[2] = {0.f, 0.f};                  // row sums over this thread's columns
       for (int j = 0; j < u.n_kv; ++j, ++g) {
         if (!wait_all(&s_full[x], g & 1)) { ok = false; break; }
         tc_fence_after();
         uint32_t r[64];
-        tmem_ld64(t_s, r);
+        tmem_ld_16x256b_x16(t_s, r);
         tmem_wait_ld();
-        const int c0 = j * kAttnBN + hf * 64;  // local key index of r[0]
-        const bool need_mask = (c0 + 64 > s.kv_len) || (s.diag != kNoDiag && c0 + 63 > q0 + s.diag);
+        const int c0 = j * kAttnBN;  // local key index of column 0
+        const bool need_mask =
+            (c0 + kAttnBN > s.kv_len) || (s.diag != kNoDiag && c0 + kAttnBN - 1 > q0 + s.diag);
         if (need_mask) {
-          const int last = min(s.kv_len - 1, lim) - c0;  // visible columns of this half: i <= last
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (i > last) r[i] = 0xff800000u;  // -inf
-        }
-        // exchange the partial row max with the other half of the tile
-        const float pm = half_max(r);
-        float* xm = xmax + ((g & 1) * 4 + x * 2) * 128;
-        xm[hf * 128 + row] = pm;
-        mbar_arrive(&xch[x]);
-        if (!wait_all(&xch[x], g & 1)) { ok = false; break; }
-        const float mx = fmaxf(pm, xm[(1 - hf) * 128 + row]) * c;
-        float alpha = 1.f;
-        bool resc = false;
-        if (mx > m_ref + kTau) {
-          if (m_ref != -INFINITY) {
-            alpha = ex2_approx(m_ref - mx);
-            resc = true;
+          for (int i = 0; i < 2; ++i) {
+            const int last = min(s.kv_len - 1, lim[i]) - c0 - cq;  // visible: 8k + e <= last
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+#pragma unroll
+              for (int e = 0; e < 2; ++e)
+                if (8 * k + e > last) r[4 * k + 2 * i + e] = 0xff800000u;  // -inf
           }
-          m_ref = mx;
         }
-        const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref;
-        const float sum = exp_half(r, c2, nb, t_s);
-        l = l * alpha + sum;
+        float alpha[2] = {1.f, 1.f};
+        bool resc = false;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float mx = row_max4(r, i) * c;
+          if (mx > m_ref[i] + kTau) {
+            if (m_ref[i] != -INFINITY) {
+              alpha[i] = ex2_approx(m_ref[i] - mx);
+              resc = true;
+            }
+            m_ref[i] = mx;
+          }
+        }
+        const float nb0 = m_ref[0] == -INFINITY ? 0.f : -m_ref[0];
+        const float nb1 = m_ref[1] == -INFINITY ? 0.f : -m_ref[1];
+        float sum[2];
+        exp_tile(r, c2, nb0, nb1, t_s, sum);
+        l[0] = l[0] * alpha[0] + sum[0];
+        l[1] = l[1] * alpha[1] + sum[1];
         if (__any_sync(0xffffffffu, resc)) {
           // S_x(j) complete => P V of tile j-1 complete: O_x is stable
 #pragma unroll
           for (int cc = 0; cc < D / 64; ++cc) {
             uint32_t w[32];
-            tmem_ld32(t_o + cc * 32, w);
+            tmem_ld_16x256b_x8(t_o + cc * 64, w);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
-            tmem_st32(t_o + cc * 32, w);
+            for (int i = 0; i < 32; ++i)
+              w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha[(i >> 1) & 1]);
+            tmem_st_16x256b_x8(t_o + cc * 64, w);
           }
         }
         tmem_wait_st();
@@ -407,46 +435,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         mbar_arrive(&p_full[x]);
       }
       if (!ok) break;
-      // epilogue: combine the two partial row sums, then each half stores its half of O
-      float* xs = xsum + x * 2 * 128;
-      xs[hf * 128 + row] = l;
-      mbar_arrive(&xl[x]);
-      if (!wait_all(&xl[x], units & 1)) { ok = false; break; }
-      const float lt = l + xs[(1 - hf) * 128 + row];
+      // epilogue: full row sums from the four threads of each row, then O / l and the lse
+      float inv_l[2], lse[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float lt = l[i];
+        lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+        inv_l[i] = lt > 0.f ? 1.0f / lt : 0.f;
+        lse[i] = lt > 0.f ? (m_ref[i] + lg2_approx(lt)) * kLn2 : -INFINITY;
+      }
       if (!wait_all(&pv_done[x], units & 1)) { ok = false; break; }  // committed once per unit
       ++units;
       tc_fence_after();
-      const float inv_l = lt > 0.f ? 1.0f / lt : 0.f;
-      const float lse = lt > 0.f ? (m_ref + lg2_approx(lt)) * kLn2 : -INFINITY;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t o[32];
-        tmem_ld32(t_o + cc * 32, o);
+        tmem_ld_16x256b_x8(t_o + cc * 64, o);
         tmem_wait_ld();
         if (cc == D / 64 - 1) {
           tc_fence_before();
           mbar_arrive(&o_empty[x]);
         }
-        if (row_valid) {
-          if (p.o_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.o) + o_elem + cc * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(
-                  pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
-                  pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
-                  pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
-                  pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(s.o) + o_elem + cc * 32);
+        for (int i = 0; i < 2; ++i) {
+          if (!row_valid[i]) continue;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(o[4 * i + 0]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                   __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+          for (int k = 0; k < 8; ++k) {
+            const float v0 = __uint_as_float(o[4 * k + 2 * i]) * inv_l[i];
+            const float v1 = __uint_as_float(o[4 * k + 2 * i + 1]) * inv_l[i];
+            const long long at = o_elem[i] + cc * 64 + 8 * k + cq;
+            if (p.o_bf16) reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(s.o) + at)[0] = pack_bf16x2(v0, v1);
+            else reinterpret_cast<float2*>(static_cast<float*>(s.o) + at)[0] = make_float2(v0, v1);
           }
         }
       }
-      if (row_valid && hf == 0 && s.lse) s.lse[orow * s.o_heads + u.h] = lse;
+      if ((lane & 3) == 0 && s.lse) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (row_valid[i]) s.lse[lse_at[i]] = lse[i];
+      }
     }
   }
 

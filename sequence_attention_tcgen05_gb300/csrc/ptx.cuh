@@ -172,12 +172,12 @@ __device__ __forceinline__ void mma_group_qk4(uint32_t d_tmem, uint32_t a_lo, ui
   asm volatile("{\n\t.reg .pred pz, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 pz, 0, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pz;\n\tadd.u32 alo, %1, 2;\n\tadd.u32 blo, %2, 2;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 4;\n\tadd.u32 blo, %2, 4;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 6;\n\tadd.u32 blo, %2, 6;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc) : "memory");
 }
 
-// O (+)= P V over the 128 keys of a tile, issued as one block: P from TMEM (keys 0-63 at columns
-// p_tmem + [0, 32), keys 64-127 at p_tmem + [64, 96)), V from shared memory (MN-major, K-step kk
-// adds kk * 128 in 16-byte units to b_lo); the first K-step accumulates iff acc_first != 0.
+// O (+)= P V over the 128 keys of a tile, issued as one block: P from TMEM (keys 2c, 2c+1 packed
+// in column p_tmem + c, c < 64), V from shared memory (MN-major, K-step kk adds kk * 128 in
+// 16-byte units to b_lo); the first K-step accumulates iff acc_first != 0.
 __device__ __forceinline__ void mma_group_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t b_lo,
                                              uint32_t hi, uint32_t idesc, uint32_t acc_first) {
-  asm volatile("{\n\t.reg .pred pf, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 db;\n\tsetp.ne.b32 pf, %5, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pf;\n\tadd.u32 alo, %1, 8;\n\tadd.u32 blo, %2, 128;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 16;\n\tadd.u32 blo, %2, 256;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 24;\n\tadd.u32 blo, %2, 384;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 64;\n\tadd.u32 blo, %2, 512;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 72;\n\tadd.u32 blo, %2, 640;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 80;\n\tadd.u32 blo, %2, 768;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 88;\n\tadd.u32 blo, %2, 896;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(p_tmem), "r"(b_lo), "r"(hi), "r"(idesc),
+  asm volatile("{\n\t.reg .pred pf, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 db;\n\tsetp.ne.b32 pf, %5, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pf;\n\tadd.u32 alo, %1, 8;\n\tadd.u32 blo, %2, 128;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 16;\n\tadd.u32 blo, %2, 256;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 24;\n\tadd.u32 blo, %2, 384;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 32;\n\tadd.u32 blo, %2, 512;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 40;\n\tadd.u32 blo, %2, 640;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 48;\n\tadd.u32 blo, %2, 768;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 56;\n\tadd.u32 blo, %2, 896;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(p_tmem), "r"(b_lo), "r"(hi), "r"(idesc),
                "r"(acc_first)
                : "memory");
 }
@@ -252,6 +252,32 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
 __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};"
                :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
+               : "memory");
+}
+
+// 16-lane TMEM accesses.  Thread t of a warp holds, per repetition k, for lanes base + t/4 and
+// base + t/4 + 8: .16x256b -> columns 8k + 2(t%4) + {0, 1} (registers 4k, 4k+1 for the first lane,
+// 4k+2, 4k+3 for the second); .16x128b -> column 4k + t%4 (registers 2k, 2k+1).
+__device__ __forceinline__ void tmem_ld_16x256b_x16(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_16x256b_x8(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
                : "memory");
 }
 
