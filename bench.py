@@ -49,9 +49,8 @@ NOMINAL_HBM_GBS = 8000.0
 # DRAM bytes (read + write) per launch of the partial-attention kernel from an ncu capture, with
 # the hash of the kernel sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.084160 MB + write 3.922688 MB
-    # (taken on the kernel before the K/V barrier merge; null until re-captured)
-    "flux_1024_u2": {"bytes": 89006848, "kernel_hash": "0c426f06c75cdad9"},
+    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.083648 MB + write 4.111616 MB
+    "flux_1024_u2": {"bytes": 89195264, "kernel_hash": "008284fb1c7a8631"},
 }
 
 
