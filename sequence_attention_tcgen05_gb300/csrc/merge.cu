@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __rest
                                                              void* __restrict__ o_out,
                                                              float* __restrict__ lse_out,
                                                              const __grid_constant__ MergeMap m) {
-  constexpr int kB = 4;
+  constexpr int kB = NP <= 2 ? 4 : (NP <= 4 ? 2 : 1);  // float4 slots per lane per batch
   const int lane = threadIdx.x & 31;
   const long long total = m.row0[m.n_blocks];
   const long long step = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
