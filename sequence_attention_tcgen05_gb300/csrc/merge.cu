@@ -98,8 +98,10 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
 
 // Merge with the result placed in the global layout (MergeMap): one warp per token row of one
 // head-sharded block, i.e. h_u contiguous D-vectors on both sides.  The row's placement is decoded
-// once; the lanes then stream the row's h_u * D / 4 float4 slots, four at a time, issuing the
-// partials' loads of a batch before combining them.
+// once; the lanes then stream the row's h_u * D / 4 float4 slots in batches of kB per lane (4 for
+// up to 2 partials, 2 for up to 4, else 1, so that the NP x kB float4 loads a lane keeps in flight
+// fit a register budget that leaves several blocks per SM), issuing the partials' loads of a batch
+// before combining them.
 template <int NP, bool OUT_BF16>
 __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __restrict__ o_parts,
                                                              long long o_stride,
