@@ -176,6 +176,13 @@ using namespace usp;
 
 namespace {
 
+// A ring chunk of two runs of rows that are not adjacent in the global tensor (zigzag with several
+// ring ranks); one ring rank's two zigzag pieces are adjacent and form one run.
+bool two_pieces(const Positions& ps) {
+  return ps.n_seg > 1 && ps.len[0] > 0 && ps.len[1] > 0 &&
+         int64_t(ps.start[1]) != int64_t(ps.start[0]) + int64_t(ps.len[0]) * ps.stride;
+}
+
 struct Grid {
   int B = 0, S = 0, H = 0, D = 0, U = 0, R = 0;
   usp_order_t order = USP_ORDER_CONTIGUOUS;
@@ -183,8 +190,8 @@ struct Grid {
   std::vector<int> S_r;        // ring chunk lengths
   std::vector<int> h, hoff;    // head groups
   // Q/K/V of every virtual rank can be addressed in place in the global tensor (each ring chunk is
-  // one affine run of rows); otherwise (zigzag with several ring ranks) they are first re-laid into
-  // the head-sharded workspace copies.
+  // one affine run of rows, or two equal half-chunks of whole 128-row tiles under zigzag); otherwise
+  // they are first re-laid into the head-sharded workspace copies.
   bool fused_in = true;
   // workspace layout (bytes)
   size_t off_q = 0, off_k = 0, off_v = 0, off_opart = 0, off_lpart = 0, total = 0;
@@ -237,7 +244,13 @@ usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int U, int R, usp_o
   }
   g.hoff.assign(U, 0);
   for (int u = 1; u < U; ++u) g.hoff[u] = g.hoff[u - 1] + g.h[u - 1];
-  g.fused_in = order != USP_ORDER_ZIGZAG || R == 1;
+  // Q/K/V are addressed in place unless a zigzag chunk's two half-chunks differ in length or are not
+  // whole 128-row tiles (a tile must not straddle them); then they are re-laid into the workspace.
+  g.fused_in = true;
+  for (int r = 0; r < R; ++r) {
+    const Positions& ps = g.pos[r];
+    if (two_pieces(ps) && !(ps.len[0] == ps.len[1] && ps.len[0] % kAttnBM == 0)) g.fused_in = false;
+  }
   g.elems = int64_t(B) * S * H * D;
   const int64_t rowsH = int64_t(B) * S * H;
   size_t at = 256;  // status word
@@ -415,9 +428,10 @@ usp_status_t usp_attn_partial(const void* q, const void* k, const void* v, int B
   AttnParams& p = params;
   std::memset(&p, 0, sizeof(p));
   usp_status_t st;
-  if ((st = make_qkv_map(&p.maps[0], q, H, D, Sq, B, q_row_stride, int64_t(Sq) * q_row_stride))) return st;
-  if ((st = make_qkv_map(&p.maps[1], k, H, D, Sk, B, kv_row_stride, int64_t(Sk) * kv_row_stride))) return st;
-  if ((st = make_qkv_map(&p.maps[2], v, H, D, Sk, B, kv_row_stride, int64_t(Sk) * kv_row_stride))) return st;
+  if ((st = make_qkv_map(&p.maps[0], q, H, D, Sq, 1, B, q_row_stride, 0, int64_t(Sq) * q_row_stride))) return st;
+  if ((st = make_qkv_map(&p.maps[1], k, H, D, Sk, 1, B, kv_row_stride, 0, int64_t(Sk) * kv_row_stride))) return st;
+  if ((st = make_qkv_map(&p.maps[2], v, H, D, Sk, 1, B, kv_row_stride, 0, int64_t(Sk) * kv_row_stride))) return st;
+
   p.B = B;
   p.o_bf16 = o_dt == USP_BF16;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -540,6 +554,8 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     for (int u = 0; u < U; ++u) {
       const void* base[3];
       int64_t row_stride, batch_stride;
+      int64_t piece_rows = std::max(1, g.S_r[r]), piece_stride = 0;
+      int n_pieces = 1;
       if (g.fused_in) {
         const int64_t e0 = (int64_t(g.pos[r].start[0]) * H + g.hoff[u]) * D;
         base[0] = static_cast<const uint16_t*>(q) + e0;
@@ -547,6 +563,11 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
         base[2] = static_cast<const uint16_t*>(v) + e0;
         row_stride = int64_t(g.pos[r].stride) * H * D;
         batch_stride = int64_t(S) * H * D;
+        if (two_pieces(g.pos[r])) {  // zigzag chunk: its two half-chunks
+          piece_rows = g.pos[r].len[0];
+          n_pieces = 2;
+          piece_stride = int64_t(g.pos[r].start[1] - g.pos[r].start[0]) * H * D;
+        }
       } else {
         const int64_t off = g.woff(r, u, D) * 2;
         base[0] = ws + g.off_q + off;
@@ -556,10 +577,12 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
         batch_stride = int64_t(g.S_r[r]) * row_stride;
       }
       if (B == 1) batch_stride = std::max<int64_t>(1, g.S_r[r]) * row_stride;
-      for (int t = 0; t < 3; ++t)
-        if ((st = make_qkv_map(&p.maps[map_index(r, u, t)], base[t], g.h[u], D, g.S_r[r], B, row_stride,
-                               batch_stride)))
+      for (int t = 0; t < 3; ++t) {
+        if ((st = make_qkv_map(&p.maps[map_index(r, u, t)], base[t], g.h[u], D, piece_rows, n_pieces, B,
+                               row_stride, piece_stride, batch_stride)))
           return st;
+        p.map_rows[map_index(r, u, t)] = n_pieces > 1 ? static_cast<int>(piece_rows) : 0;
+      }
     }
   }
   p.B = B;
@@ -574,6 +597,13 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     for (int kstep = 0; kstep < R; ++kstep) {
       const int r2 = (r - kstep + R) % R;
       const std::vector<Run> runs = plan_runs(g.pos[r], g.pos[r2], causal != 0);
+      // a zigzag chunk addressed in place is two maps' worth of pieces: every run must start on a
+      // 128-row tile so that no tile straddles its half-chunks (runs start at 0 or at the second
+      // half for these orderings)
+      if (g.fused_in && two_pieces(g.pos[r]))
+        for (const Run& run : runs)
+          if (run.q0 % kAttnBM != 0)
+            return fail(USP_ERR_UNSUPPORTED, "zigzag run at row %d does not start on a 128-row tile", run.q0);
       for (int u = 0; u < U; ++u) {
         for (const Run& run : runs) {
           AttnSeg s{};

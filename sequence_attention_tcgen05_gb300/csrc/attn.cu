@@ -216,26 +216,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (q_iter > 0 && !mbar_wait(q_empty, (q_iter - 1) & 1, abort_flag, p.status, budget)) break;
         mbar_arrive_expect_tx(q_full, 2 * L::kQTile);
         const int qrow = s.q_row0 + u.q0;
+        const int qn = p.map_rows[s.q_map];  // 0: one piece (4-D map)
 #pragma unroll
-        for (int x = 0; x < 2; ++x)
+        for (int x = 0; x < 2; ++x) {
+          const int row = qrow + x * kAttnBM;  // 128-row tiles never straddle two pieces
 #pragma unroll
-          for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_4d(sm + L::kQ + x * L::kQTile + blk * kAttnBM * 128, &p.maps[s.q_map], blk * 64,
-                        u.h, qrow + x * kAttnBM, u.b, q_full);
+          for (int blk = 0; blk < D / 64; ++blk) {
+            uint8_t* dst = sm + L::kQ + x * L::kQTile + blk * kAttnBM * 128;
+            if (qn == 0) tma_load_4d(dst, &p.maps[s.q_map], blk * 64, u.h, row, u.b, q_full);
+            else tma_load_5d(dst, &p.maps[s.q_map], blk * 64, u.h, row % qn, row / qn, u.b, q_full);
+          }
+        }
         ++q_iter;
         const int kvrow = s.kv_row0;
+        const int kn = p.map_rows[s.k_map];  // the K and V maps of a run have the same pieces
+        int kr = kn ? kvrow % kn : kvrow, kp = kn ? kvrow / kn : 0;  // row, piece of the next tile
         bool ok = true;
         for (int j = 0; j < u.n_kv; ++j) {
           if (!mbar_wait(&kv_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
           mbar_arrive_expect_tx(&kv_full[stage], L::kKBytes + L::kVBytes);
 #pragma unroll
-          for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_4d(sm + L::kK + stage * L::kKBytes + blk * kAttnBN * 128, &p.maps[s.k_map],
-                        blk * 64, u.h, kvrow + j * kAttnBN, u.b, &kv_full[stage]);
-#pragma unroll
-          for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_4d(sm + L::kV + stage * L::kVBytes + blk * kAttnBN * 128, &p.maps[s.v_map],
-                        blk * 64, u.h, kvrow + j * kAttnBN, u.b, &kv_full[stage]);
+          for (int blk = 0; blk < D / 64; ++blk) {
+            uint8_t* dk = sm + L::kK + stage * L::kKBytes + blk * kAttnBN * 128;
+            uint8_t* dv = sm + L::kV + stage * L::kVBytes + blk * kAttnBN * 128;
+            if (kn == 0) {
+              tma_load_4d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, u.b, &kv_full[stage]);
+              tma_load_4d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, u.b, &kv_full[stage]);
+            } else {
+              tma_load_5d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, kp, u.b, &kv_full[stage]);
+              tma_load_5d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, kp, u.b, &kv_full[stage]);
+            }
+          }
+          kr += kAttnBN;
+          if (kn && kr >= kn) { kr -= kn; ++kp; }
           ++fills[stage];
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -504,8 +517,9 @@ usp_status_t launch_one(const AttnParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D, int64_t rows,
-                          int B, int64_t row_stride, int64_t batch_stride) {
+usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D, int64_t piece_rows,
+                          int n_pieces, int B, int64_t row_stride, int64_t piece_stride,
+                          int64_t batch_stride) {
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -520,18 +534,29 @@ usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D
     return reinterpret_cast<EncodeFn>(fn);
   }();
   if (!encode) return fail(USP_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(n_heads),
-                              static_cast<cuuint64_t>(std::max<int64_t>(rows, 1)),
+  const int64_t rows = std::max<int64_t>(piece_rows, 1);
+  const int64_t pstride = std::max<int64_t>(piece_stride, rows * row_stride);
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(n_heads),
+                              static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(std::max(n_pieces, 1)),
                               static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(D) * 2,
                                  static_cast<cuuint64_t>(row_stride) * 2,
+                                 static_cast<cuuint64_t>(pstride) * 2,
                                  static_cast<cuuint64_t>(std::max<int64_t>(batch_stride, row_stride)) * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kAttnBM), 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
-                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const cuuint32_t box[5] = {64, 1, static_cast<cuuint32_t>(kAttnBM), 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r;
+  if (n_pieces <= 1) {  // {D, heads, rows, B}: the piece dimension dropped
+    const cuuint64_t dims4[4] = {dims[0], dims[1], dims[2], dims[4]};
+    const cuuint64_t strides3[3] = {strides[0], strides[1], strides[3]};
+    r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims4, strides3, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return fail(USP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   return USP_OK;
 }

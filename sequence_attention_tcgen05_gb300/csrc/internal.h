@@ -128,6 +128,7 @@ struct AttnSeg {
 
 struct AttnParams {
   CUtensorMap maps[kAttnMaxMaps];
+  int map_rows[kAttnMaxMaps];  // two-piece maps: rows per piece (row l = piece l / n, row l % n); 0: one piece
   AttnSeg segs[kAttnMaxSegs];
   int n_segs;
   int n_units;
@@ -146,10 +147,14 @@ struct Run {
 // causal = false gives one run covering everything.
 std::vector<Run> plan_runs(const Positions& qp, const Positions& kp, bool causal);
 
-// 4-D tensor map {D, n_heads, rows, B} over bf16 data: heads adjacent (D elements apart), rows
-// row_stride elements apart, batches batch_stride elements apart.
-usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D, int64_t rows,
-                          int B, int64_t row_stride, int64_t batch_stride);
+// 5-D tensor map {D, n_heads, piece_rows, n_pieces, B} over bf16 data: heads adjacent (D elements
+// apart), rows row_stride elements apart, pieces piece_stride apart, batches batch_stride apart.
+// Map row l is row l % piece_rows of piece l / piece_rows: one piece (encoded as the 4-D map
+// {D, n_heads, rows, B}) for a chunk that is one run of rows, two for a zigzag chunk (its two
+// half-chunks) addressed in place.  Box: 64 x 1 x 128 (x 1) x 1.
+usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D, int64_t piece_rows,
+                          int n_pieces, int B, int64_t row_stride, int64_t piece_stride,
+                          int64_t batch_stride);
 
 // Launch over all segments (split into several launches if there are more than fit).
 usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs, int D,

@@ -75,6 +75,13 @@ def test_workspace_size(L):
     # zigzag ring: additionally the head-sharded bf16 copies of Q, K, V
     z = usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3, "zigzag")
     assert z >= r + 3 * 1000 * 4 * 64 * 2
+    # zigzag with equal half-chunks of whole 128-row tiles (64K tokens, ring 8: 16 x 4096) is
+    # addressed in place: the same size as contiguous order, no copies
+    zc = usp.usp_attention_workspace_size(1, 65536, 32, 128, 1, 8, "contiguous")
+    zz = usp.usp_attention_workspace_size(1, 65536, 32, 128, 1, 8, "zigzag")
+    assert zz == zc
+    # half-chunks of 4095.5 rows on average (65535 tokens) are not whole tiles: copies again
+    assert usp.usp_attention_workspace_size(1, 65535, 32, 128, 1, 8, "zigzag") > zc
     assert usp.usp_attention_workspace_size(1, 10, 4, 96, 1, 1) == 0
     assert usp.usp_attention_workspace_size(1, 10, 4, 64, 5, 4) == 0
 

@@ -58,6 +58,25 @@ def test_grid_small(U, R, order, causal):
     check_attention(o, l, ro, rl, f"grid U={U} R={R} {order} causal={causal}")
 
 
+@pytest.mark.parametrize("B,S,H,D,U,R,causal", [
+    (1, 512, 4, 64, 1, 2, True),      # half-chunks of 128 rows: one tile each
+    (2, 2048, 4, 128, 2, 4, True),    # half-chunks of 256 rows, Ulysses 2 x ring 4
+    (1, 3072, 3, 128, 1, 3, True),    # half-chunks of 512 rows, ring 3
+    (2, 1024, 4, 64, 2, 2, False),    # non-causal zigzag
+])
+def test_zigzag_in_place_half_chunks(B, S, H, D, U, R, causal):
+    """Zigzag ring chunks of two equal half-chunks of whole 128-row tiles are read in place by
+    two-piece tensor maps (no workspace copy); checked element by element against the oracle."""
+    assert S % (2 * R) == 0 and (S // (2 * R)) % 128 == 0
+    o, l, (qb, kb, vb) = run_usp(B, S, H, D, U, R, causal, "zigzag", seed=S + R)
+    ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), 1 / math.sqrt(D), causal)
+    check_attention(o, l, ro, rl, f"zigzag in place S={S} U={U} R={R} causal={causal}")
+    ws = usp.usp_attention_workspace_size(B, S, H, D, U, R, "zigzag", usp.USP_FP32)
+    # status word + ring partials only: no Q/K/V copies
+    rows_h = B * S * H
+    assert ws < 256 + R * (rows_h * D * 4 + rows_h * 4) + 4096 * R + 2 ** 20
+
+
 def test_uneven_seq_lens_and_bf16_out():
     S, U, R = 1001, 2, 2
     ring = oracle.default_split(S, R)
