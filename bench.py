@@ -193,12 +193,15 @@ def workload(name: str):
 def phase_bytes(w, out_elem: int):
     """Algorithmic HBM bytes of the bandwidth-bound phases (each element read once + written once).
 
-    Q/K/V are re-laid by a separate pass only for zigzag order with several ring ranks (otherwise
-    the attention's tensor maps address each virtual rank's head-sharded view in place); O and LSE
-    are always written in the global layout by the attention (one ring rank) or the merge."""
+    Q/K/V are re-laid by a separate pass only for zigzag order with several ring ranks whose
+    half-chunks are unequal or not whole 128-row tiles (otherwise the attention's tensor maps
+    address each virtual rank's head-sharded view in place); O and LSE are always written in the
+    global layout by the attention (one ring rank) or the merge."""
     elems = w.B * w.S * w.H * w.D
     rows_h = w.B * w.S * w.H
-    qkv_pass = w.order == "zigzag" and w.ring_degree > 1
+    half = w.S // (2 * w.ring_degree)
+    qkv_pass = (w.order == "zigzag" and w.ring_degree > 1 and
+                (w.S % (2 * w.ring_degree) != 0 or half % 128 != 0))
     b = {"qkv_relayout": 2 * 3 * elems * 2 if qkv_pass else 0}
     if w.ring_degree > 1:
         b["merge"] = w.ring_degree * (elems * 4 + rows_h * 4) + elems * out_elem + rows_h * 4
