@@ -204,10 +204,30 @@ def phase_bytes(w, out_elem: int):
                 (w.S % (2 * w.ring_degree) != 0 or half % 128 != 0))
     b = {"qkv_relayout": 2 * 3 * elems * 2 if qkv_pass else 0}
     if w.ring_degree > 1:
-        b["merge"] = w.ring_degree * (elems * 4 + rows_h * 4) + elems * out_elem + rows_h * 4
+        # every partial's LSE is read; only partials whose rows saw a key are read in full (a
+        # fully masked chunk pair leaves lse = -inf and the merge skips its O)
+        seen = w.B * visible_partial_vectors(w)
+        b["merge"] = w.ring_degree * rows_h * 4 + seen * w.D * 4 + elems * out_elem + rows_h * 4
     else:
         b["merge"] = 0
     return b
+
+
+def visible_partial_vectors(w) -> int:
+    """(row, head) vectors of one batch whose ring-step partial saw at least one key, from the
+    library's host-side chunk-pair planner (usp_plan_pairs: q rows, visible kv rows and the
+    diagonal of every run)."""
+    from sequence_attention_tcgen05_gb300 import usp
+    U = w.ulysses_degree
+    heads = [w.H // U + (1 if u < w.H % U else 0) for u in range(U)]
+    total = 0
+    for (u, _r, _k, _r2, _row0, q_rows, kv_rows, diag) in usp.usp_plan_pairs(
+            w.S, U, w.ring_degree, w.causal, w.order):
+        if kv_rows <= 0:
+            continue
+        rows = q_rows if diag == 2**31 - 1 else max(0, q_rows - max(0, -diag))
+        total += rows * heads[u]
+    return total
 
 
 def gpu_head_start(us: float = 60.0):
