@@ -49,8 +49,8 @@ NOMINAL_HBM_GBS = 8000.0
 # DRAM bytes (read + write) per launch of the partial-attention kernel from an ncu capture, with
 # the hash of the kernel sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.083648 MB + write 4.111616 MB
-    "flux_1024_u2": {"bytes": 89195264, "kernel_hash": "008284fb1c7a8631"},
+    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.077248 MB + write 4.077312 MB
+    "flux_1024_u2": {"bytes": 89154560, "kernel_hash": "d6191b3f1c540a10"},
 }
 
 
