@@ -167,10 +167,11 @@ usp_status_t usp_lse_merge(int n_parts, const float* o_parts, int64_t o_part_str
  *   workspace: device scratch of at least usp_attention_workspace_size(...) bytes, 256-byte
  *   aligned.  Its first 4 bytes are the status word usp_check_status reads and clears; zero
  *   them once before the first call (e.g. allocate the workspace zeroed).
- *   Steps (one stream): (1) the seq->head re-layout of Q, K, V: when every ring chunk is one
- *   affine run of global rows (contiguous or stripe order, or one ring rank) each virtual rank's
- *   head-sharded view is addressed in place by the attention's tensor maps; for zigzag with
- *   several ring ranks a fused reorder + seq->head pass copies Q, K, V into the workspace first.
+ *   Steps (one stream): (1) the seq->head re-layout of Q, K, V: each virtual rank's head-sharded
+ *   view is addressed in place by the attention's tensor maps when its ring chunk is one affine
+ *   run of global rows (contiguous or stripe order, one ring rank) or, under zigzag, two equal
+ *   half-chunks of whole 128-row tiles (S divisible by 256 * ring_degree); otherwise a fused
+ *   reorder + seq->head pass copies Q, K, V into the workspace first.
  *   (2) One partial-attention launch over every (ring step, chunk pair, head, query block), with
  *   fully masked causal tiles skipped.  (3) With several ring ranks, the LSE merge of the ring
  *   partials.  The head->seq re-layout and inverse reorder of O and LSE are the store addressing
