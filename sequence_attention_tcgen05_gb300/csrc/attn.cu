@@ -271,8 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0, q_iter = 0, units_done = 0;
       uint32_t gp[2] = {0, 0};  // P V count per query tile
       bool ok = true;
-      // Shared-memory descriptors (128-byte swizzle, SBO 1024 B, version 1): constant high word;
-      // low word = start address >> 4 | LBO field (1 for the K-major Q and K, 16384 B for V).
+      // Shared-memory matrix descriptors (tcgen05 descriptor version 1): bits 0-13 start address
+      // >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte offset >> 4 (1024 B: 8-row atoms),
+      // 46-47 version 1, 49-51 base offset 0 (atoms 1024-byte aligned), 61-63 layout 2 (128-byte
+      // swizzle).  The high word is the same for every operand; low word = start address >> 4 |
+      // LBO field (1 for the K-major Q and K, 16384 B between V's 64-column blocks).
       constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
       const uint32_t q_lo = (q_base >> 4) | (1u << 16);
       const uint32_t k_lo = (k_base >> 4) | (1u << 16);
