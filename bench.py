@@ -17,6 +17,9 @@ loop whose events sit between the phases.  Times come from CUDA events on the la
   e2e       the same metric through the C ABI with the inputs in pinned host memory: each step
             copies Q, K, V host->device, runs usp_attention and copies O and LSE back.
   roofline  the partial-attention phase alone against the measured dense bf16 tensor peak.
+  relayout_merge  GB/s of the step's bandwidth-bound phases, plus separately timed standalone
+            measurements of the re-layout entry points on the workload's tensors and of the LSE
+            merge entry point on two ring partials of the workload's size.
 
 Multi-GPU: the method is partitioned onto virtual ranks of one GPU, so N GPUs run N independent
 replicas (weak scaling); the only cross-rank traffic is the timing reduction.
@@ -289,6 +292,43 @@ def standalone_relayout(w, q, k, v, o, flush, stream, reps: int = 50):
                            "us": t_out / reps * 1e3}}
 
 
+def standalone_merge(w, out_dt, flush, stream, reps: int = 30):
+    """GB/s of the standalone usp_lse_merge entry point on two fp32 ring partials of this
+    workload's size (a separately timed measurement: Ulysses-only workloads have no merge in the
+    step).  Bytes: both partials and their LSE read, O (out_dt) and LSE written."""
+    import torch
+
+    from sequence_attention_tcgen05_gb300 import usp
+    rows, H, D = w.B * w.S, w.H, w.D
+    g = torch.Generator(device="cuda").manual_seed(1)
+    o_parts = torch.randn((2, rows, H, D), dtype=torch.float32, device="cuda", generator=g)
+    l_parts = torch.randn((2, rows, H), dtype=torch.float32, device="cuda", generator=g)
+    o_out = torch.empty((rows, H, D), dtype=out_dt, device="cuda")
+    l_out = torch.empty((rows, H), dtype=torch.float32, device="cuda")
+
+    def call():
+        usp.usp_lse_merge(2, o_parts, rows * H * D, l_parts, rows * H, rows, H, D, o_out, l_out,
+                          stream=stream)
+
+    call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t = 0.0
+    for i in range(reps + 3):
+        flush()
+        gpu_head_start()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            t += e0.elapsed_time(e1)
+    elems, rows_h = rows * H * D, rows * H
+    nbytes = 2 * (elems * 4 + rows_h * 4) + elems * o_out.element_size() + rows_h * 4
+    us = t / reps * 1e3
+    del o_parts, l_parts, o_out, l_out
+    return {"partials": 2, "bytes": nbytes, "us": us, "GB/s": nbytes / (us * 1e-6) / 1e9}
+
+
 def cpu_oracle_sample(w, target_s: float, rng_seed: int = 0):
     """Time the fp64 oracle on whole heads of the workload (all query rows of a head against its
     full key set) until about ``target_s`` seconds have passed or every head is done; returns
@@ -498,9 +538,10 @@ def run_ours(args):
                         "frac_measured_hbm": gbs / peaks["hbm_gbs"], "frac_8TBs": gbs / NOMINAL_HBM_GBS}
     bw_bytes = sum(pb.values())
     standalone = standalone_relayout(w, q, k, v, o, flush, stream)
-    for part in ("seq2head_qkv", "head2seq_o"):
-        standalone[part]["frac_measured_hbm"] = standalone[part]["GB/s"] / peaks["hbm_gbs"]
-        standalone[part]["frac_8TBs"] = standalone[part]["GB/s"] / NOMINAL_HBM_GBS
+    standalone_m = standalone_merge(w, out_dt, flush, stream)
+    for part in (standalone["seq2head_qkv"], standalone["head2seq_o"], standalone_m):
+        part["frac_measured_hbm"] = part["GB/s"] / peaks["hbm_gbs"]
+        part["frac_8TBs"] = part["GB/s"] / NOMINAL_HBM_GBS
     bw_s = sum(phases[n] for n in ("qkv_relayout", "merge")) / 1000.0 / breakdown_steps
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -516,7 +557,8 @@ def run_ours(args):
         "relayout_merge": {"GB/s": bw_bytes / bw_s / 1e9 if bw_s > 0 else None,
                            "frac_measured_hbm": (bw_bytes / bw_s / 1e9 / peaks["hbm_gbs"]) if bw_s > 0 else None,
                            "frac_8TBs": (bw_bytes / bw_s / 1e9 / NOMINAL_HBM_GBS) if bw_s > 0 else None,
-                           "phases": bw, "standalone_relayout": standalone},
+                           "phases": bw, "standalone_relayout": standalone,
+                           "standalone_merge": standalone_m},
         "phases_ms_per_step": {k: v / breakdown_steps for k, v in phases.items()},
         "phases_steps": breakdown_steps,
         "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
