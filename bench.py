@@ -52,10 +52,8 @@ NOMINAL_HBM_GBS = 8000.0
 # DRAM bytes (read + write) per launch of the partial-attention kernel from an ncu capture, with
 # the hash of the kernel sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.077248 MB + write 4.077312 MB
-    # (captured on sources d6191b3f1c540a10; bdb371eb5d39b6cf only drops unused PTX helpers and
-    # edits comments: the compiled kernel is the same)
-    "flux_1024_u2": {"bytes": 89154560, "kernel_hash": "bdb371eb5d39b6cf"},
+    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.094400 MB + write 4.450304 MB
+    "flux_1024_u2": {"bytes": 89544704, "kernel_hash": "2aec0a238eb2a426"},
 }
 
 

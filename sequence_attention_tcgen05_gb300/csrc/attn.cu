@@ -4,7 +4,10 @@
 //
 // One persistent CTA per SM, five warpgroups (640 threads):
 //   WG0  warp 0: TMA producer — the unit's two 128-row Q tiles, then K and V tiles into a
-//                STAGES-deep ring (K and V of a key tile serve both query tiles).
+//                STAGES-deep ring (K and V of a key tile serve both query tiles).  A K slot is
+//                released when both score MMAs of its tile complete, a V slot when both P V MMAs
+//                do, so the next K load starts about a period before the V load; the MMA thread
+//                waits once per key tile, on both.
 //        warp 1: MMA issuer (one thread) and TMEM owner.  Per key tile j, in this order:
 //                  S_a = Q_a K_j^T,  O_b += P_b(j-1) V_{j-1},  S_b = Q_b K_j^T,  O_a += P_a(j) V_j
 //                (SS MMA M=128 N=128 for the scores; TS MMA with P read from TMEM for P V), so the
@@ -18,11 +21,14 @@
 //                wait for each other.  Masking on boundary tiles, 2^(s * scale log2e - m) with packed
 //                fp32x2 fused multiply-adds and MUFU ex2; each thread's column pair becomes one
 //                bf16x2 P word that a .16x128b tcgen05.st puts exactly at P column 4k + t%4, so P
-//                for the tile's 128 keys is packed over S_x columns [0, 64).  The running max m is
-//                raised only when a tile's max exceeds it by more than 8 (log2 units); then the
-//                thread rescales its part of O in TMEM.  Otherwise the stale max stays, which bounds
-//                P by 2^8 and is exact after the final division by the row sum.  Epilogue: O / l
-//                (fp32 or bf16) and lse = (m + log2 l) ln 2 stored from the same fragments.
+//                for the tile's 128 keys is packed over S_x columns [0, 64).  Once a warp's rows
+//                have a finite running max m, a tile is exponentiated against that (stale) m with
+//                no max over the tile; only when a thread's partial row sum exceeds 2^16 (or is not
+//                finite) does the warp take the slow path: row maxima, m raised where the tile's
+//                max exceeds it by more than 8 (log2 units), its part of O rescaled in TMEM and
+//                the exponentials redone.  P stays bounded by 2^16, and the stale m is exact after
+//                the final division by the row sum.  Epilogue: O / l (fp32 or bf16) and
+//                lse = (m + log2 l) ln 2 stored from the same fragments.
 // Without a max exchange between the warpgroups the softmax term of the chain
 // S_x(j) -> softmax -> O_x += P V -> S_x(j+1), which sets the kernel's period per key tile, is
 // one warpgroup's own work.
@@ -46,7 +52,8 @@
 namespace usp {
 namespace {
 
-constexpr float kTau = 8.0f;  // lazy-rescale threshold, log2 units
+constexpr float kTau = 8.0f;          // slow path: raise m by at least this much (log2 units)
+constexpr float kFastSum = 65536.0f;  // fast path: a thread's partial row sum of one tile
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kThreads = 640;
 constexpr int kSoftmaxThreads = 256;  // the two warpgroups of one query tile
@@ -65,9 +72,9 @@ struct Layout {
   static constexpr int kK = kQ + 2 * kQTile;
   static constexpr int kV = kK + STAGES * kKBytes;
   static constexpr int kBar = kV + STAGES * kVBytes;
-  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2], o_empty[2],
-  // mma_done
-  static constexpr int kNumBars = 2 + 2 * STAGES + 9;
+  // q_full, q_empty, kv_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], pv_done[2],
+  // o_empty[2], mma_done
+  static constexpr int kNumBars = 2 + 3 * STAGES + 9;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
@@ -165,8 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
   uint64_t* kv_full = bars + 2;  // K and V of a stage, one transaction count
-  uint64_t* kv_empty = kv_full + STAGES;
-  uint64_t* s_full = kv_empty + STAGES;  // [2]: query tile a, b
+  uint64_t* k_empty = kv_full + STAGES;  // K slot free: both score MMAs of its tile completed
+  uint64_t* v_empty = k_empty + STAGES;  // V slot free: both P V MMAs of its tile completed
+  uint64_t* s_full = v_empty + STAGES;  // [2]: query tile a, b
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_empty = pv_done + 2;
@@ -184,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mbar_init(q_empty, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -233,23 +242,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         int kr = kn ? kvrow % kn : kvrow, kp = kn ? kvrow / kn : 0;  // row, piece of the next tile
         bool ok = true;
         for (int j = 0; j < u.n_kv; ++j) {
-          if (!mbar_wait(&kv_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
+          // K(j) may overwrite K(j - STAGES) once its score MMAs are done, well before the P V
+          // MMAs release V(j - STAGES); one transaction count covers both.
+          if (!mbar_wait(&k_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
           mbar_arrive_expect_tx(&kv_full[stage], L::kKBytes + L::kVBytes);
 #pragma unroll
           for (int blk = 0; blk < D / 64; ++blk) {
             uint8_t* dk = sm + L::kK + stage * L::kKBytes + blk * kAttnBN * 128;
+            if (kn == 0) tma_load_4d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, u.b, &kv_full[stage]);
+            else tma_load_5d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, kp, u.b, &kv_full[stage]);
+          }
+          ++fills[stage];  // counted now: on an abort before the V loads, the drain covers K
+          if (!mbar_wait(&v_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
+#pragma unroll
+          for (int blk = 0; blk < D / 64; ++blk) {
             uint8_t* dv = sm + L::kV + stage * L::kVBytes + blk * kAttnBN * 128;
-            if (kn == 0) {
-              tma_load_4d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, u.b, &kv_full[stage]);
-              tma_load_4d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, u.b, &kv_full[stage]);
-            } else {
-              tma_load_5d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, kp, u.b, &kv_full[stage]);
-              tma_load_5d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, kp, u.b, &kv_full[stage]);
-            }
+            if (kn == 0) tma_load_4d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, u.b, &kv_full[stage]);
+            else tma_load_5d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, kp, u.b, &kv_full[stage]);
           }
           kr += kAttnBN;
           if (kn && kr >= kn) { kr -= kn; ++kp; }
-          ++fills[stage];
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -315,9 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           qk(0, stage);
           if (j > 0) {
             if (!pv(1, prev_stage, j == 1, false)) { ok = false; break; }
-            mma_commit(&kv_empty[prev_stage]);
+            mma_commit(&v_empty[prev_stage]);
           }
           qk(1, stage);
+          mma_commit(&k_empty[stage]);
           if (j == u.n_kv - 1) mma_commit(q_empty);
           if (!pv(0, stage, j == 0, j == u.n_kv - 1)) { ok = false; break; }
           prev_stage = stage;
@@ -325,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         if (!ok) break;
         if (!pv(1, prev_stage, u.n_kv == 1, true)) { ok = false; break; }
-        mma_commit(&kv_empty[prev_stage]);
+        mma_commit(&v_empty[prev_stage]);
         ++units_done;
       }
       // drain: all issued MMAs complete before TMEM is freed
@@ -416,21 +429,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         float alpha[2] = {1.f, 1.f};
         bool resc = false;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const float mx = row_max4(r, i) * c;
-          if (mx > m_ref[i] + kTau) {
-            if (m_ref[i] != -INFINITY) {
-              alpha[i] = ex2_approx(m_ref[i] - mx);
-              resc = true;
-            }
-            m_ref[i] = mx;
-          }
-        }
-        const float nb0 = m_ref[0] == -INFINITY ? 0.f : -m_ref[0];
-        const float nb1 = m_ref[1] == -INFINITY ? 0.f : -m_ref[1];
         float sum[2];
-        exp_tile(r, c2, nb0, nb1, t_s, sum);
+        // Fast path: exponentials against the running max as it stands.  A partial sum above
+        // kFastSum (or inf / NaN) means some score rose more than 11 log2 units above m: wait
+        // for the P stores, then redo the tile after raising m.
+        bool fast = __all_sync(0xffffffffu, m_ref[0] != -INFINITY && m_ref[1] != -INFINITY);
+        if (fast) {
+          exp_tile(r, c2, -m_ref[0], -m_ref[1], t_s, sum);
+          fast = __all_sync(0xffffffffu, sum[0] <= kFastSum && sum[1] <= kFastSum);
+          if (!fast) tmem_wait_st();
+        }
+        if (!fast) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float mx = row_max4(r, i) * c;
+            if (mx > m_ref[i] + kTau) {
+              if (m_ref[i] != -INFINITY) {
+                alpha[i] = ex2_approx(m_ref[i] - mx);
+                resc = true;
+              }
+              m_ref[i] = mx;
+            }
+          }
+          const float nb0 = m_ref[0] == -INFINITY ? 0.f : -m_ref[0];
+          const float nb1 = m_ref[1] == -INFINITY ? 0.f : -m_ref[1];
+          exp_tile(r, c2, nb0, nb1, t_s, sum);
+        }
         l[0] = l[0] * alpha[0] + sum[0];
         l[1] = l[1] * alpha[1] + sum[1];
         if (__any_sync(0xffffffffu, resc)) {

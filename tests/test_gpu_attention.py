@@ -12,11 +12,14 @@ from gpu_util import Guarded, check_attention, to_dev_bf16, torch, widen
 pytestmark = pytest.mark.gpu
 
 
-def run_partial(B, H, Sq, Sk, D, q_pos=None, k_pos=None, seed=0, out="fp32", packed=False):
+def run_partial(B, H, Sq, Sk, D, q_pos=None, k_pos=None, seed=0, out="fp32", packed=False,
+                k_row_scale=None):
     t = torch()
     qb = synth.make_tensor_bits(seed, 0, B, Sq, H, D)
     kb = synth.make_tensor_bits(seed, 1, B, Sk, H, D)
     vb = synth.make_tensor_bits(seed, 2, B, Sk, H, D)
+    if k_row_scale is not None:  # key row t multiplied by k_row_scale[t] in fp32, then bf16 again
+        kb = synth.bf16_bits(synth.bf16_to_f32(kb) * np.float32(k_row_scale)[None, :, None, None])
     if packed:
         # q, k, v rows interleaved as [B][S][3][H][D] (QKV-packed layout): row stride 3*H*D
         assert Sq == Sk
@@ -100,3 +103,39 @@ def test_repeat_calls_identical():
     a = run_partial(1, 4, 640, 900, 128, seed=9)
     b = run_partial(1, 4, 640, 900, 128, seed=9)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def key_profile(kind, Sk):
+    t = np.arange(Sk, dtype=np.float64)
+    if kind == "rising":    # key norms grow 16x along the keys: the row max climbs tile after tile
+        return 2.0 ** (4.0 * t / Sk)
+    if kind == "falling":   # the first tiles dominate: later exponentials are tiny against m
+        return 2.0 ** (4.0 * (1.0 - t / Sk))
+    f = np.ones(Sk)         # a few large keys late in the row
+    f[[260, 261, 500, 777, 901, Sk - 10]] = 20.0
+    return f
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("kind", ["rising", "falling", "spikes"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_running_max_changes(D, kind, causal):
+    """Scores that rise far above the first key tile's maximum force the softmax's slow path
+    (running max raised, O rescaled in TMEM, exponentials redone); falling scores keep a stale
+    maximum far above later tiles.  Both are exact after the final division by the row sum."""
+    Sq, Sk = 300, 1100
+    f = key_profile(kind, Sk)
+    qspec = ([(800, Sq)], 1) if causal else None
+    kspec = ([(0, Sk)], 1) if causal else None
+    o, l, q, k, v, scale = run_partial(1, 2, Sq, Sk, D, qspec, kspec, seed=11, k_row_scale=f)
+    s = np.einsum("bqhd,bkhd->bhqk", q, k) * scale / math.log(2.0)  # log2 units
+    if causal:
+        s = np.where(positions(kspec)[None, None, None, :] <= positions(qspec)[None, None, :, None],
+                     s, -np.inf)
+    climb = s.max(axis=-1) - s[..., :128].max(axis=-1)
+    if kind != "falling":
+        assert (climb > 11.0).mean() > 0.5, "inputs do not reach the slow path"
+    ro, rl = oracle.attention(q, k, v, scale, causal,
+                              positions(qspec) if causal else None,
+                              positions(kspec) if causal else None)
+    check_attention(o, l, ro, rl, f"{kind} causal={causal} D={D}")
