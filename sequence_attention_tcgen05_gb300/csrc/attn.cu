@@ -6,9 +6,11 @@
 //   WG0  warp 0: TMA producer — the unit's two 128-row Q tiles, then K and V tiles into a
 //                STAGES-deep ring (K and V of a key tile serve both query tiles).  A K slot is
 //                released when both score MMAs of its tile complete, a V slot when both P V MMAs
-//                do, so the next K load starts about a period before the V load; the MMA thread
+//                do, so the next K load starts about a period before the V load; the MMA warp
 //                waits once per key tile, on both.
-//        warp 1: MMA issuer (one thread) and TMEM owner.  Per key tile j, in this order:
+//        warp 1: MMA issuer and TMEM owner.  The whole warp runs the issuing loop (its state
+//                stays warp-uniform); one elected lane issues each tcgen05.mma and commit.  Per
+//                key tile j, in this order:
 //                  S_a = Q_a K_j^T,  O_b += P_b(j-1) V_{j-1},  S_b = Q_b K_j^T,  O_a += P_a(j) V_j
 //                (SS MMA M=128 N=128 for the scores; TS MMA with P read from TMEM for P V), so the
 //                softmax of each query tile overlaps a score MMA and a P V MMA of the other tile.
@@ -33,7 +35,7 @@
 // S_x(j) -> softmax -> O_x += P V -> S_x(j+1), which sets the kernel's period per key tile, is
 // one warpgroup's own work.
 // TMEM (512 columns): S_a [0,128) S_b [128,256) O_a [256,256+D) O_b [256+D,256+2D); P_x packed in
-// columns [0,64) of S_x.  MMAs issued by one thread execute in issue order, so a completed
+// columns [0,64) of S_x.  MMAs issued by the one issuing lane execute in issue order, so a completed
 // S_x(j) implies P V of tile j-1 of the same query tile has completed: S_x may then be read, P_x
 // rewritten and O_x rescaled without another wait.
 //
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* mma_done = o_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbort);
-  const int warp = threadIdx.x >> 5;
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);  // uniform
   const int lane = threadIdx.x & 31;
   const int wg = warp >> 2;
   const uint64_t budget = p.budget_ns;
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       }
       if (q_iter) mbar_drain(q_full, (q_iter - 1) & 1, drain_budget);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kAttnBM, kAttnBN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kAttnBM, D, 1);
@@ -283,6 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0, q_iter = 0, units_done = 0;
       uint32_t gp[2] = {0, 0};  // P V count per query tile
       bool ok = true;
+      // Every lane waits; the vote keeps the warp's control flow uniform even if a wait times out
+      // on some lanes only.
+      auto wait_w = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status, budget));
+      };
       // Shared-memory matrix descriptors (tcgen05 descriptor version 1): bits 0-13 start address
       // >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte offset >> 4 (1024 B: 8-row atoms),
       // 46-47 version 1, 49-51 base offset 0 (atoms 1024-byte aligned), 61-63 layout 2 (128-byte
@@ -303,9 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // one (pv_done tells the epilogue that O_x is final).  P_x: keys 0-63 packed in S_x columns
       // [0,32), keys 64-127 in [64,96).  V(st) arrived with K(st): the S MMA of this stage waited.
       auto pv = [&](int x, uint32_t st, bool first, bool last) -> bool {
-        if (!mbar_wait(&p_full[x], gp[x] & 1, abort_flag, p.status, budget)) return false;
+        if (!wait_w(&p_full[x], gp[x] & 1)) return false;
         if (first && units_done > 0 &&
-            !mbar_wait(&o_empty[x], (units_done - 1) & 1, abort_flag, p.status, budget))
+            !wait_w(&o_empty[x], (units_done - 1) & 1))
           return false;
         tc_fence_after();
         mma_group_pv(tmem + 256 + x * D, tmem + x * 128, v_lo + st * (L::kVBytes >> 4), kDescHi,
@@ -319,11 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (u.n_kv == 0) continue;
         // Q and K/V come from TMA (async proxy, like the MMAs): the barrier waits order them, no
         // tcgen05 fence is needed; P comes from tcgen05.st of other threads (fence in pv()).
-        if (!mbar_wait(q_full, q_iter & 1, abort_flag, p.status, budget)) break;
+        if (!wait_w(q_full, q_iter & 1)) break;
         ++q_iter;
         uint32_t prev_stage = 0;
         for (int j = 0; j < u.n_kv; ++j) {
-          if (!mbar_wait(&kv_full[stage], phase, abort_flag, p.status, budget)) { ok = false; break; }
+          if (!wait_w(&kv_full[stage], phase)) { ok = false; break; }
           qk(0, stage);
           if (j > 0) {
             if (!pv(1, prev_stage, j == 1, false)) { ok = false; break; }

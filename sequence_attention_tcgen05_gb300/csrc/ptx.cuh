@@ -128,12 +128,16 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// The MMA groups and the commit below are warp-wide: all 32 lanes of a converged warp execute
+// them with the same operands, and the lane `elect.sync` picks issues the tcgen05 instructions.
+// Running the issuing role on a whole warp keeps its loop state and descriptors warp-uniform.
+
 // S = A B^T over K = 128 (the 8 K-steps of a 128x128 score tile), issued as one block:
 // a_lo / b_lo are the low descriptor words of the K-step-0 operands (start address >> 4 | LBO field),
 // hi the shared high word; K-step kk adds (kk / 4) * 1024 + (kk % 4) * 2 (16-byte units) to both.
 __device__ __forceinline__ void mma_group_qk8(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                               uint32_t hi, uint32_t idesc) {
-  asm volatile("{\n\t.reg .pred pz, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 pz, 0, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pz;\n\tadd.u32 alo, %1, 2;\n\tadd.u32 blo, %2, 2;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 4;\n\tadd.u32 blo, %2, 4;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 6;\n\tadd.u32 blo, %2, 6;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1024;\n\tadd.u32 blo, %2, 1024;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1026;\n\tadd.u32 blo, %2, 1026;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1028;\n\tadd.u32 blo, %2, 1028;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1030;\n\tadd.u32 blo, %2, 1030;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc) : "memory");
+  asm volatile("{\n\t.reg .pred ee;\n\telect.sync _|ee, 0xffffffff;\n\t.reg .pred pz, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 pz, 0, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pz;\n\tadd.u32 alo, %1, 2;\n\tadd.u32 blo, %2, 2;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 4;\n\tadd.u32 blo, %2, 4;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 6;\n\tadd.u32 blo, %2, 6;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1024;\n\tadd.u32 blo, %2, 1024;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1026;\n\tadd.u32 blo, %2, 1026;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1028;\n\tadd.u32 blo, %2, 1028;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 1030;\n\tadd.u32 blo, %2, 1030;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc) : "memory");
 }
 
 // S = A B^T over K = 64 (the 4 K-steps of a 128x128 score tile), issued as one block:
@@ -141,7 +145,7 @@ __device__ __forceinline__ void mma_group_qk8(uint32_t d_tmem, uint32_t a_lo, ui
 // hi the shared high word; K-step kk adds (kk / 4) * 1024 + (kk % 4) * 2 (16-byte units) to both.
 __device__ __forceinline__ void mma_group_qk4(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                               uint32_t hi, uint32_t idesc) {
-  asm volatile("{\n\t.reg .pred pz, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 pz, 0, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pz;\n\tadd.u32 alo, %1, 2;\n\tadd.u32 blo, %2, 2;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 4;\n\tadd.u32 blo, %2, 4;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 6;\n\tadd.u32 blo, %2, 6;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc) : "memory");
+  asm volatile("{\n\t.reg .pred ee;\n\telect.sync _|ee, 0xffffffff;\n\t.reg .pred pz, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 pz, 0, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pz;\n\tadd.u32 alo, %1, 2;\n\tadd.u32 blo, %2, 2;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 4;\n\tadd.u32 blo, %2, 4;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\tadd.u32 alo, %1, 6;\n\tadd.u32 blo, %2, 6;\n\tmov.b64 da, {alo, %3};\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc) : "memory");
 }
 
 // O (+)= P V over the 128 keys of a tile, issued as one block: P from TMEM (keys 2c, 2c+1 packed
@@ -149,15 +153,16 @@ __device__ __forceinline__ void mma_group_qk4(uint32_t d_tmem, uint32_t a_lo, ui
 // 16-byte units to b_lo); the first K-step accumulates iff acc_first != 0.
 __device__ __forceinline__ void mma_group_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t b_lo,
                                              uint32_t hi, uint32_t idesc, uint32_t acc_first) {
-  asm volatile("{\n\t.reg .pred pf, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 db;\n\tsetp.ne.b32 pf, %5, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pf;\n\tadd.u32 alo, %1, 8;\n\tadd.u32 blo, %2, 128;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 16;\n\tadd.u32 blo, %2, 256;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 24;\n\tadd.u32 blo, %2, 384;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 32;\n\tadd.u32 blo, %2, 512;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 40;\n\tadd.u32 blo, %2, 640;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 48;\n\tadd.u32 blo, %2, 768;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 56;\n\tadd.u32 blo, %2, 896;\n\tmov.b64 db, {blo, %3};\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(p_tmem), "r"(b_lo), "r"(hi), "r"(idesc),
+  asm volatile("{\n\t.reg .pred ee;\n\telect.sync _|ee, 0xffffffff;\n\t.reg .pred pf, pa;\n\t.reg .b32 alo, blo;\n\t.reg .b64 db;\n\tsetp.ne.b32 pf, %5, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\tadd.u32 alo, %1, 0;\n\tadd.u32 blo, %2, 0;\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pf;\n\tadd.u32 alo, %1, 8;\n\tadd.u32 blo, %2, 128;\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 16;\n\tadd.u32 blo, %2, 256;\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 24;\n\tadd.u32 blo, %2, 384;\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 32;\n\tadd.u32 blo, %2, 512;\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 40;\n\tadd.u32 blo, %2, 640;\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 48;\n\tadd.u32 blo, %2, 768;\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\tadd.u32 alo, %1, 56;\n\tadd.u32 blo, %2, 896;\n\tmov.b64 db, {blo, %3};\n\t@ee tcgen05.mma.cta_group::1.kind::f16 [%0], [alo], db, %4, pa;\n\t}" ::"r"(d_tmem), "r"(p_tmem), "r"(b_lo), "r"(hi), "r"(idesc),
                "r"(acc_first)
                : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
+// Arrive once on `bar` (from the elected lane) when every tcgen05 operation the warp's issuing
+// lane issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n\t.reg .pred ee;\n\telect.sync _|ee, 0xffffffff;\n\t@ee tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_u32(bar))
       : "memory");
 }
