@@ -4,16 +4,18 @@
 //
 // One persistent CTA per SM, five warpgroups (640 threads):
 //   WG0  warp 0: TMA producer — the unit's two 128-row Q tiles, then K and V tiles into a
-//                STAGES-deep ring (K and V of a key tile serve both query tiles).  A K slot is
-//                released when both score MMAs of its tile complete, a V slot when both P V MMAs
-//                do, so the next K load starts about a period before the V load; the MMA warp
-//                waits once per key tile, on both.
+//                STAGES-deep ring (K and V of a key tile serve both query tiles).  K and V have
+//                their own full and empty barriers: a K slot is released when both score MMAs of
+//                its tile complete, a V slot when both P V MMAs do, so the next K load starts
+//                about a period before the V load.
 //        warp 1: MMA issuer and TMEM owner.  The whole warp runs the issuing loop (its state
 //                stays warp-uniform); one elected lane issues each tcgen05.mma and commit.  Per
 //                key tile j, in this order:
 //                  S_a = Q_a K_j^T,  O_b += P_b(j-1) V_{j-1},  S_b = Q_b K_j^T,  O_a += P_a(j) V_j
 //                (SS MMA M=128 N=128 for the scores; TS MMA with P read from TMEM for P V), so the
 //                softmax of each query tile overlaps a score MMA and a P V MMA of the other tile.
+//                The waits for V_j and K_{j+1} come just before the wait for P_a(j), the long one,
+//                so that O_a += P_a(j) V_j is followed at once by S_a = Q_a K_{j+1}^T.
 //        warps 2-3 idle.  The warpgroup gives registers away (setmaxnreg) to the softmax groups.
 //   WG1..WG4  softmax of query tile x = (wg-1)/2 over lane half h = (wg-1)%2 of every 32-lane TMEM
 //                quadrant: each thread owns two rows of the tile (quadrant lanes 16h + t/4 and that
@@ -74,9 +76,9 @@ struct Layout {
   static constexpr int kK = kQ + 2 * kQTile;
   static constexpr int kV = kK + STAGES * kKBytes;
   static constexpr int kBar = kV + STAGES * kVBytes;
-  // q_full, q_empty, kv_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], pv_done[2],
-  // o_empty[2], mma_done
-  static constexpr int kNumBars = 2 + 3 * STAGES + 9;
+  // q_full, q_empty, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2],
+  // pv_done[2], o_empty[2], mma_done
+  static constexpr int kNumBars = 2 + 4 * STAGES + 9;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
@@ -173,8 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;  // K and V of a stage, one transaction count
-  uint64_t* k_empty = kv_full + STAGES;  // K slot free: both score MMAs of its tile completed
+  uint64_t* k_full = bars + 2;
+  uint64_t* v_full = k_full + STAGES;
+  uint64_t* k_empty = v_full + STAGES;  // K slot free: both score MMAs of its tile completed
   uint64_t* v_empty = k_empty + STAGES;  // V slot free: both P V MMAs of its tile completed
   uint64_t* s_full = v_empty + STAGES;  // [2]: query tile a, b
   uint64_t* p_full = s_full + 2;
@@ -193,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
     }
@@ -218,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------------- TMA producer
       uint32_t stage = 0, phase = 0, q_iter = 0;
-      uint32_t fills[STAGES];
-      for (int s = 0; s < STAGES; ++s) fills[s] = 0;
+      uint32_t kfills[STAGES], vfills[STAGES];
+      for (int s = 0; s < STAGES; ++s) kfills[s] = vfills[s] = 0;
       for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
@@ -245,23 +249,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         bool ok = true;
         for (int j = 0; j < u.n_kv; ++j) {
           // K(j) may overwrite K(j - STAGES) once its score MMAs are done, well before the P V
-          // MMAs release V(j - STAGES); one transaction count covers both.
+          // MMAs release V(j - STAGES).
           if (!mbar_wait(&k_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
-          mbar_arrive_expect_tx(&kv_full[stage], L::kKBytes + L::kVBytes);
+          mbar_arrive_expect_tx(&k_full[stage], L::kKBytes);
 #pragma unroll
           for (int blk = 0; blk < D / 64; ++blk) {
             uint8_t* dk = sm + L::kK + stage * L::kKBytes + blk * kAttnBN * 128;
-            if (kn == 0) tma_load_4d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, u.b, &kv_full[stage]);
-            else tma_load_5d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, kp, u.b, &kv_full[stage]);
+            if (kn == 0) tma_load_4d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, u.b, &k_full[stage]);
+            else tma_load_5d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, kp, u.b, &k_full[stage]);
           }
-          ++fills[stage];  // counted now: on an abort before the V loads, the drain covers K
+          ++kfills[stage];
           if (!mbar_wait(&v_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
+          mbar_arrive_expect_tx(&v_full[stage], L::kVBytes);
 #pragma unroll
           for (int blk = 0; blk < D / 64; ++blk) {
             uint8_t* dv = sm + L::kV + stage * L::kVBytes + blk * kAttnBN * 128;
-            if (kn == 0) tma_load_4d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, u.b, &kv_full[stage]);
-            else tma_load_5d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, kp, u.b, &kv_full[stage]);
+            if (kn == 0) tma_load_4d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, u.b, &v_full[stage]);
+            else tma_load_5d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, kp, u.b, &v_full[stage]);
           }
+          ++vfills[stage];
           kr += kAttnBN;
           if (kn && kr >= kn) { kr -= kn; ++kp; }
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -269,9 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!ok) break;
       }
       for (int s = 0; s < STAGES; ++s) {
-        if (fills[s]) {
-          mbar_drain(&kv_full[s], (fills[s] - 1) & 1, drain_budget);
-        }
+        if (kfills[s]) mbar_drain(&k_full[s], (kfills[s] - 1) & 1, drain_budget);
+        if (vfills[s]) mbar_drain(&v_full[s], (vfills[s] - 1) & 1, drain_budget);
       }
       if (q_iter) mbar_drain(q_full, (q_iter - 1) & 1, drain_budget);
     } else if (warp == 1) {
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       };
       // O_x += P_x V(st); `first` = first key tile of the unit (overwrites O_x), `last` = its last
       // one (pv_done tells the epilogue that O_x is final).  P_x: keys 0-63 packed in S_x columns
-      // [0,32), keys 64-127 in [64,96).  V(st) arrived with K(st): the S MMA of this stage waited.
+      // [0,32), keys 64-127 in [64,96).  V(st) was waited for before the first P V of its tile.
       auto pv = [&](int x, uint32_t st, bool first, bool last) -> bool {
         if (!wait_w(&p_full[x], gp[x] & 1)) return false;
         if (first && units_done > 0 &&
@@ -329,8 +334,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!wait_w(q_full, q_iter & 1)) break;
         ++q_iter;
         uint32_t prev_stage = 0;
+        if (!wait_w(&k_full[stage], phase)) break;
+        // K(j) was waited for before this iteration; V(j) and K(j+1) are waited for just before the
+        // wait for P_a(j), which is the long one, so that O_a += P_a V is followed directly by
+        // S_a = Q_a K(j+1)^T.
         for (int j = 0; j < u.n_kv; ++j) {
-          if (!wait_w(&kv_full[stage], phase)) { ok = false; break; }
           qk(0, stage);
           if (j > 0) {
             if (!pv(1, prev_stage, j == 1, false)) { ok = false; break; }
@@ -339,9 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           qk(1, stage);
           mma_commit(&k_empty[stage]);
           if (j == u.n_kv - 1) mma_commit(q_empty);
+          const uint32_t ns = stage + 1 == STAGES ? 0 : stage + 1;
+          const uint32_t nph = ns == 0 ? phase ^ 1 : phase;
+          if (!wait_w(&v_full[stage], phase)) { ok = false; break; }
+          if (j + 1 < u.n_kv && !wait_w(&k_full[ns], nph)) { ok = false; break; }
           if (!pv(0, stage, j == 0, j == u.n_kv - 1)) { ok = false; break; }
           prev_stage = stage;
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          stage = ns;
+          phase = nph;
         }
         if (!ok) break;
         if (!pv(1, prev_stage, u.n_kv == 1, true)) { ok = false; break; }
