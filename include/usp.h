@@ -229,7 +229,12 @@ size_t usp_attention_workspace_size(int B, int S, int H, int D, int ulysses_degr
 
 /* Synchronises `stream`, reads the device status word at `status` (a usp_attention workspace or
  * the uint32 given to usp_attn_partial), clears it, and returns USP_ERR_TIMEOUT if a bounded wait
- * gave up since the last check, USP_ERR_CUDA if the stream reports an error, else USP_OK. */
+ * gave up since the last check, USP_ERR_CUDA if the stream reports an error, else USP_OK.
+ * Every device-side wait of the attention kernel gives up after USP_WAIT_BUDGET_MS milliseconds
+ * (environment, read at each call; default 2000); all its roles then stop, finish their copies
+ * and MMAs in flight, free their tensor memory and exit, so the context stays usable.
+ * USP_TEST_WITHHOLD_LOADS=1 (environment, read at each call) is a test hook for that path: the
+ * kernel's producer issues no loads, so the waits run out. */
 usp_status_t usp_check_status(void* status, usp_stream_t stream);
 
 /* Host-only planning query (no device needed): the chunk-pair work list usp_attention launches,

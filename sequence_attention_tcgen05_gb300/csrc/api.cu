@@ -25,6 +25,13 @@ unsigned long long wait_budget_ns() {
   return kDefaultBudgetNs;
 }
 
+// Test hook for the failure path: USP_TEST_WITHHOLD_LOADS=1 makes the attention kernel's producer
+// issue no loads, so the other roles' bounded waits run out and the status word reports it.
+int withhold_loads() {
+  const char* s = std::getenv("USP_TEST_WITHHOLD_LOADS");
+  return (s && s[0] == '1' && s[1] == 0) ? 1 : 0;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 }  // namespace
 
@@ -437,6 +444,7 @@ usp_status_t usp_attn_partial(const void* q, const void* k, const void* v, int B
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.budget_ns = wait_budget_ns();
+  p.withhold_loads = withhold_loads();
   Positions qp, kp;
   if (q_pos) {
     qp.n_seg = q_pos->n_seg; kp.n_seg = k_pos->n_seg;
@@ -589,6 +597,7 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.budget_ns = wait_budget_ns();
+  p.withhold_loads = withhold_loads();
   // ring partials (fp32, head-sharded W layout) when R > 1; else the final output in place
   const int64_t slot_o = g.elems * 4, slot_l = int64_t(B) * S * H;
   p.o_bf16 = R > 1 ? 0 : (o_dt == USP_BF16);

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0, q_iter = 0;
       uint32_t kfills[STAGES], vfills[STAGES];
       for (int s = 0; s < STAGES; ++s) kfills[s] = vfills[s] = 0;
-      for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
+      for (int unit = p.withhold_loads ? p.n_units : blockIdx.x; unit < p.n_units; unit += gridDim.x) {
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
         const AttnSeg& s = *u.seg;

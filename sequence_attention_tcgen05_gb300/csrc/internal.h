@@ -137,6 +137,7 @@ struct AttnParams {
   float scale_log2;
   uint32_t* status;
   unsigned long long budget_ns;
+  int withhold_loads;  // test hook: the producer issues no loads, so every wait runs out
 };
 
 // A run of query rows produced by the chunk-pair planner.

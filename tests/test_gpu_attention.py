@@ -1,5 +1,6 @@
 """usp_attn_partial (tcgen05 kernel) against the fp64 oracle on the same seeded bf16 inputs."""
 import math
+import time
 
 import numpy as np
 import pytest
@@ -139,3 +140,34 @@ def test_running_max_changes(D, kind, causal):
                               positions(qspec) if causal else None,
                               positions(kspec) if causal else None)
     check_attention(o, l, ro, rl, f"{kind} causal={causal} D={D}")
+
+
+def test_bounded_wait_runs_out_then_context_usable(monkeypatch):
+    """The failure path of the bounded device waits, without a fault: with the test hook
+    USP_TEST_WITHHOLD_LOADS=1 the kernel's producer issues no loads, so every other role's wait
+    runs out after USP_WAIT_BUDGET_MS; all roles stop and free their tensor memory, nothing is
+    written outside the outputs, and usp_check_status reports USP_ERR_TIMEOUT.  The same context
+    then computes the next call correctly."""
+    t = torch()
+    B, H, Sq, Sk, D = 1, 2, 300, 400, 128
+    q = to_dev_bf16(synth.make_tensor_bits(3, 0, B, Sq, H, D))
+    k = to_dev_bf16(synth.make_tensor_bits(3, 1, B, Sk, H, D))
+    v = to_dev_bf16(synth.make_tensor_bits(3, 2, B, Sk, H, D))
+    o = Guarded((B, Sq, H, D), t.float32)
+    lse = Guarded((B, Sq, H), t.float32)
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    monkeypatch.setenv("USP_WAIT_BUDGET_MS", "50")
+    monkeypatch.setenv("USP_TEST_WITHHOLD_LOADS", "1")
+    t0 = time.monotonic()
+    usp.usp_attn_partial(q, k, v, B, H, Sq, Sk, D, H * D, H * D, 1.0 / math.sqrt(D), o.view, lse.view,
+                         status=status)
+    assert usp.usp_check_status(status) == usp.USP_ERR_TIMEOUT
+    assert time.monotonic() - t0 < 10.0
+    o.check()
+    lse.check()
+    monkeypatch.delenv("USP_TEST_WITHHOLD_LOADS")
+    monkeypatch.delenv("USP_WAIT_BUDGET_MS")
+    assert usp.usp_check_status(status) == usp.USP_OK  # cleared by the previous check
+    o2, l2, q2, k2, v2, scale = run_partial(B, H, Sq, Sk, D, seed=3)
+    ro, rl = oracle.attention(q2, k2, v2, scale)
+    check_attention(o2, l2, ro, rl, "after a timed-out call")
