@@ -363,6 +363,26 @@ def cores() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name; on Arm, implementer and part)."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if ":" in line:
+                    key, val = (x.strip() for x in line.split(":", 1))
+                    fields.setdefault(key, val)
+    except OSError:
+        pass
+    if fields.get("model name"):
+        return fields["model name"]
+    if "CPU part" in fields:
+        return (f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} "
+                f"part {fields['CPU part']}")
+    return platform.machine()
+
+
 # ------------------------------------------------------------------------------------------------
 # arms
 # ------------------------------------------------------------------------------------------------
@@ -387,7 +407,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w, "fp64"),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "cpu": cpu_model()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -567,7 +587,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cv, cdt, desc = cpu_oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": cv, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
-                                "sample": desc, "seconds": cdt}
+                                "sample": desc, "seconds": cdt, "cpu": cpu_model()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
