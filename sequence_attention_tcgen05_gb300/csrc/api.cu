@@ -667,6 +667,7 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
         mm.p_stride[kb] = g.pos[r].stride;
       }
     }
+    mm.all_seen = causal ? 0 : 1;
     mm.vec0[R * U] = int64_t(B) * S * H;
     mm.row0[R * U] = mm.row0[R * U - 1] + int64_t(B) * g.S_r[R - 1];
     if ((st = launch_lse_merge(R, reinterpret_cast<const float*>(ws + g.off_opart), g.elems,

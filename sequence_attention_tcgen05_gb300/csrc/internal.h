@@ -86,6 +86,7 @@ struct MergeMap {
   int S_r[kMergeMaxBlocks], h[kMergeMaxBlocks], hoff[kMergeMaxBlocks];
   int p_start0[kMergeMaxBlocks], p_len0[kMergeMaxBlocks], p_start1[kMergeMaxBlocks],
       p_stride[kMergeMaxBlocks];
+  int all_seen;  // no partial can be empty (non-causal): load every partial with its LSE
 };
 
 usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_stride,

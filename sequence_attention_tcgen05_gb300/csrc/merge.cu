@@ -101,8 +101,10 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
 // once; the lanes then stream the row's h_u * D / 4 float4 slots in batches of kB per lane (4 for
 // up to 2 partials, 2 for up to 4, else 1, so that the NP x kB float4 loads a lane keeps in flight
 // fit a register budget that leaves several blocks per SM), issuing the partials' loads of a batch
-// before combining them.
-template <int NP, bool OUT_BF16>
+// before combining them.  Without a causal mask (ALL_SEEN) every partial slot holds a result, so a
+// partial's loads go out together with its LSE load; otherwise a partial is loaded only once its
+// LSE shows that its rows saw a key.
+template <int NP, bool OUT_BF16, bool ALL_SEEN>
 __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __restrict__ o_parts,
                                                              long long o_stride,
                                                              const float* __restrict__ lse_parts,
@@ -142,16 +144,22 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __rest
         head[i] = f / qpv;
         q[i] = f - head[i] * qpv;
 #pragma unroll
-        for (int k = 0; k < NP; ++k)
+        for (int k = 0; k < NP; ++k) {
           l_[i][k] = f < nf4 ? __ldg(lse_parts + k * lse_stride + src_vec + head[i]) : -INFINITY;
-      }
-#pragma unroll
-      for (int i = 0; i < kB; ++i)
-#pragma unroll
-        for (int k = 0; k < NP; ++k)
-          if (l_[i][k] != -INFINITY)
+          if (ALL_SEEN && f < nf4)  // every slot was written: load it with its LSE, not after
             o_[i][k] = __ldcs(reinterpret_cast<const float4*>(o_parts + k * o_stride +
                                                               (src_vec + head[i]) * D) + q[i]);
+        }
+      }
+      if (!ALL_SEEN) {
+#pragma unroll
+        for (int i = 0; i < kB; ++i)
+#pragma unroll
+          for (int k = 0; k < NP; ++k)
+            if (l_[i][k] != -INFINITY)
+              o_[i][k] = __ldcs(reinterpret_cast<const float4*>(o_parts + k * o_stride +
+                                                                (src_vec + head[i]) * D) + q[i]);
+      }
 #pragma unroll
       for (int i = 0; i < kB; ++i) {
         if (f0 + i * 32 + lane >= nf4) continue;
@@ -202,12 +210,16 @@ void launch_np(bool out_bf16, const MergeMap* map, unsigned blocks, cudaStream_t
     long long rb = (map->row0[map->n_blocks] + 7) / 8;
     if (rb > 152LL * 32) rb = 152LL * 32;
     const unsigned nb = static_cast<unsigned>(std::max(1LL, rb));
-    if (out_bf16)
-      lse_merge_rows_kernel<NP, true><<<nb, 256, 0, stream>>>(o_parts, o_stride, lse_parts,
-                                                              lse_stride, D, o_out, lse_out, *map);
-    else
-      lse_merge_rows_kernel<NP, false><<<nb, 256, 0, stream>>>(o_parts, o_stride, lse_parts,
-                                                               lse_stride, D, o_out, lse_out, *map);
+    auto go = [&](auto kern) {
+      kern<<<nb, 256, 0, stream>>>(o_parts, o_stride, lse_parts, lse_stride, D, o_out, lse_out, *map);
+    };
+    if (map->all_seen) {
+      if (out_bf16) go(lse_merge_rows_kernel<NP, true, true>);
+      else go(lse_merge_rows_kernel<NP, false, true>);
+    } else {
+      if (out_bf16) go(lse_merge_rows_kernel<NP, true, false>);
+      else go(lse_merge_rows_kernel<NP, false, false>);
+    }
     return;
   }
   if (out_bf16)
