@@ -15,7 +15,10 @@ loop whose events sit between the phases.  Times come from CUDA events on the la
   value     attention TFLOP/s of the whole step: algorithmic FLOPs 4 B H D x (visible query/key
             pairs) over the step's device time (all phases), summed over ranks.
   e2e       the same metric through the C ABI with the inputs in pinned host memory: each step
-            copies Q, K, V host->device, runs usp_attention and copies O and LSE back.
+            copies Q, K, V host->device, runs usp_attention and copies O and LSE back.  `value` is
+            pipelined as a caller serving a stream of requests runs it (two device buffer sets;
+            step i's copy-in overlaps step i-1's attention and copy-out); `serial_value` runs one
+            step at a time on one stream.
   roofline  the partial-attention phase alone against the measured dense bf16 tensor peak.
   relayout_merge  GB/s of the step's bandwidth-bound phases, plus separately timed standalone
             measurements of the re-layout entry points on the workload's tensors and of the LSE
@@ -521,6 +524,7 @@ def run_ours(args):
     e2e_steps = max(3, min(args.steps, 50))
     o_host = torch.empty(o.shape, dtype=out_dt).pin_memory()
     l_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    # (a) serial: one step at a time on one stream (copy in, usp_attention, copy out)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
     for i in range(e2e_steps + 1):
@@ -536,7 +540,52 @@ def run_ours(args):
         e_end.synchronize()
         if i > 0:
             e2e_ms += e_start.elapsed_time(e_end)
-    e2e_value, _ = aggregate(e2e_steps * flops, e2e_ms / 1000.0, world, device)
+    e2e_serial, _ = aggregate(e2e_steps * flops, e2e_ms / 1000.0, world, device)
+    # (b) pipelined, as a caller serving a stream of requests runs it: two sets of device buffers,
+    # one stream per direction of the host link (the two directions overlap) and one for compute.
+    # Every step still copies its Q, K, V in and its O, LSE out inside the timed region; step i's
+    # copy-in overlaps step i-1's attention and copy-out.
+    sets = [(q, k, v, o, lse, o_host, l_host),
+            (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(o),
+             torch.empty_like(lse), torch.empty(o.shape, dtype=out_dt).pin_memory(),
+             torch.empty(lse.shape, dtype=torch.float32).pin_memory())]
+    s_in, s_cmp, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("in", "cmp", "out")}
+    for b_ in range(2):
+        ev["cmp"][b_].record(s_cmp)
+        ev["out"][b_].record(s_out)
+
+    def pipelined(n_steps):
+        for i in range(n_steps):
+            b_ = i & 1
+            qd, kd, vd, od, ld, oh, lh = sets[b_]
+            s_in.wait_event(ev["cmp"][b_])  # step i-2's attention has read this input set
+            with torch.cuda.stream(s_in):
+                for dst, src in zip((qd, kd, vd), host):
+                    dst.copy_(src, non_blocking=True)
+            ev["in"][b_].record(s_in)
+            s_cmp.wait_event(ev["in"][b_])
+            s_cmp.wait_event(ev["out"][b_])  # step i-2's copy-out has read this output set
+            usp.usp_attention(qd, kd, vd, B, S, H, D, scale, w.causal, w.ulysses_degree,
+                              w.ring_degree, od, ld, ws, nbytes, seq, None, w.order, o_code, s_cmp)
+            ev["cmp"][b_].record(s_cmp)
+            s_out.wait_event(ev["cmp"][b_])
+            with torch.cuda.stream(s_out):
+                oh.copy_(od, non_blocking=True)
+                lh.copy_(ld, non_blocking=True)
+            ev["out"][b_].record(s_out)
+
+    pipelined(4)
+    torch.cuda.synchronize()
+    p_start, p_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p_start.record(s_in)
+    pipelined(e2e_steps)
+    p_end.record(s_out)  # after the last copy-out, which depends on every earlier operation
+    p_end.synchronize()
+    e2e_value, _ = aggregate(e2e_steps * flops, p_start.elapsed_time(p_end) / 1000.0, world, device)
+    if usp.usp_check_status(ws, s_cmp) != usp.USP_OK:
+        raise RuntimeError("device status after the end-to-end loops: " +
+                           usp.lib().usp_last_error().decode())
     h2d = 3 * B * S * H * D * 2
     d2h = B * S * H * D * out_elem + B * S * H * 4
 
@@ -580,7 +629,10 @@ def run_ours(args):
         "phases_ms_per_step": {k: v / breakdown_steps for k, v in phases.items()},
         "phases_steps": breakdown_steps,
         "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "mode": "pipelined: step i's copy-in overlaps step i-1's attention and copy-out "
+                        "(two device buffer sets, one stream per link direction)",
+                "serial_value": e2e_serial / 1e12},
         "gpu_launches": launches,
         "clocks": clk,
     }
