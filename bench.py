@@ -55,8 +55,8 @@ NOMINAL_HBM_GBS = 8000.0
 # DRAM bytes (read + write) per launch of the partial-attention kernel from an ncu capture, with
 # the hash of the kernel sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.126912 MB + write 4.142336 MB
-    "flux_1024_u2": {"bytes": 89269248, "kernel_hash": "8b224e61387f65a4"},
+    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.138432 MB + write 4.126464 MB
+    "flux_1024_u2": {"bytes": 89264896, "kernel_hash": "15fcae45c593c630"},
 }
 
 

@@ -395,30 +395,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const AttnSeg& s = *u.seg;
       const int q0 = u.q0 + x * kAttnBM;  // first local row of this query tile
       bool row_valid[2];
-      long long o_elem[2], lse_at[2];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        row_valid[i] = rw[i] < u.qv[x];
+      for (int i = 0; i < 2; ++i) row_valid[i] = rw[i] < u.qv[x];
+      // output element of row i's column 0 and its LSE index (computed where used, so that they
+      // are not live across the key-tile loop)
+      auto out_at = [&](int i, long long& oe, long long& la) {
         const int ol = s.o_row0 + q0 + rw[i];  // output-side local row
         const long long opos = ol < s.o_len0
                                    ? static_cast<long long>(s.o_start0) + static_cast<long long>(ol) * s.o_stride
                                    : static_cast<long long>(s.o_start1) + static_cast<long long>(ol - s.o_len0) * s.o_stride;
         const long long orow = static_cast<long long>(u.b) * s.o_bstride + opos;
-        o_elem[i] = (orow * s.o_heads + u.h) * D;
-        lse_at[i] = orow * s.o_heads + u.h;
-      }
+        la = orow * s.o_heads + u.h;
+        oe = la * D;
+      };
       if (u.n_kv == 0) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (!row_valid[i]) continue;
+          long long o_elem_i, lse_at_i;
+          out_at(i, o_elem_i, lse_at_i);
           for (int k = 0; k < D / 8; ++k) {
             if (p.o_bf16) {
-              reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(s.o) + o_elem[i] + 8 * k + cq)[0] = 0u;
+              reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(s.o) + o_elem_i + 8 * k + cq)[0] = 0u;
             } else {
-              reinterpret_cast<float2*>(static_cast<float*>(s.o) + o_elem[i] + 8 * k + cq)[0] = make_float2(0.f, 0.f);
+              reinterpret_cast<float2*>(static_cast<float*>(s.o) + o_elem_i + 8 * k + cq)[0] = make_float2(0.f, 0.f);
             }
           }
-          if ((lane & 3) == 0 && s.lse) s.lse[lse_at[i]] = -INFINITY;
+          if ((lane & 3) == 0 && s.lse) s.lse[lse_at_i] = -INFINITY;
         }
         continue;
       }
@@ -508,6 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!wait_all(&pv_done[x], units & 1)) { ok = false; break; }  // committed once per unit
       ++units;
       tc_fence_after();
+      long long o_elem[2], lse_at[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) out_at(i, o_elem[i], lse_at[i]);
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t o[32];
