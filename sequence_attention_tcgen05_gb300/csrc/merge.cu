@@ -4,7 +4,8 @@
 //   m = max_k lse_k,  w_k = 2^((lse_k - m) log2 e),  out = sum w_k out_k / sum w_k,
 //   lse = m + ln(sum w_k),
 // which is exact in real arithmetic and equal to applying the pairwise form in ring order.
-// Partials with lse = -inf saw no key: they get weight 0 and their out is never read.
+// Partials with lse = -inf saw no key: they get weight 0, and their out is not read (except by
+// the rows variant without a causal mask, which loads every slot with its LSE and ignores it).
 //
 // HBM-bound: each thread owns float4 slots of D-vectors (a warp reads 512 contiguous bytes of each
 // partial for D = 128; the LSE loads of a vector are warp-uniform broadcasts).  The partial count
