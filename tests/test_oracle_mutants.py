@@ -1,0 +1,219 @@
+"""Planted mistakes in the oracle (on the CPU): every plausible error in its arithmetic must be
+caught by at least one pin of the kind ``tests/test_oracle_*.py`` uses (pure-Python brute force
+without a max shift, torch's fp64 SDPA, closed forms, invariants), while the real oracle passes all
+of them.  This shows that the pins discriminate, not only that they pass."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle.usp as ousp
+
+RNG = np.random.default_rng(77)
+NEG_INF = float("-inf")
+
+
+# ------------------------------------------------------------------------------------------------
+# attention pins (independent of the oracle's formula)
+# ------------------------------------------------------------------------------------------------
+
+def _brute(q, k, v, scale, allowed):
+    Sq, D = q.shape
+    out = np.zeros((Sq, v.shape[1]))
+    lse = np.full(Sq, NEG_INF)
+    for i in range(Sq):
+        js = [j for j in range(k.shape[0]) if allowed[i][j]]
+        if not js:
+            continue
+        e = {j: math.exp(scale * math.fsum(q[i, d] * k[j, d] for d in range(D))) for j in js}
+        z = math.fsum(e.values())
+        lse[i] = math.log(z)
+        for d in range(v.shape[1]):
+            out[i, d] = math.fsum(e[j] * v[j, d] for j in js) / z
+    return out, lse
+
+
+def _pin_brute_force():
+    Sq, Sk, D = 6, 9, 4
+    q, k, v = (RNG.standard_normal((1, n, 1, D)) for n in (Sq, Sk, Sk))
+    scale = 1.0 / math.sqrt(D)
+    qp, kp = np.arange(Sq) + (Sk - Sq), np.arange(Sk)
+    for causal in (False, True):
+        o, l = oracle.attention(q, k, v, scale, causal, qp, kp)
+        allowed = [[(not causal) or kp[j] <= qp[i] for j in range(Sk)] for i in range(Sq)]
+        bo, bl = _brute(q[0, :, 0], k[0, :, 0], v[0, :, 0], scale, allowed)
+        assert np.allclose(o[0, :, 0], bo, rtol=1e-12, atol=1e-12)
+        assert np.allclose(l[0, :, 0], bl, rtol=1e-12, atol=1e-12)
+
+
+def _pin_torch_sdpa():
+    B, S, H, D = 1, 19, 2, 8
+    q, k, v = (RNG.standard_normal((B, S, H, D)) for _ in range(3))
+    scale = 1.0 / math.sqrt(D)
+    for causal in (False, True):
+        o, _ = oracle.attention(q, k, v, scale, causal)
+        tq, tk, tv = (torch.from_numpy(x).permute(0, 2, 1, 3) for x in (q, k, v))
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal,
+                                                               scale=scale)
+        assert np.allclose(o, ref.permute(0, 2, 1, 3).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def _pin_zero_query():
+    # Q = 0: every visible score is 0, so out = mean of the visible V rows and lse = ln |J|
+    S, D = 7, 3
+    q = np.zeros((1, S, 1, D))
+    k, v = RNG.standard_normal((1, S, 1, D)), RNG.standard_normal((1, S, 1, D))
+    o, l = oracle.attention(q, k, v, 0.5, True)
+    for i in range(S):
+        assert np.allclose(o[0, i, 0], v[0, :i + 1, 0].mean(axis=0), atol=1e-13)
+        assert abs(l[0, i, 0] - math.log(i + 1)) < 1e-13
+
+
+def _pin_single_key():
+    # one visible key: out = its V row, lse = its scaled score
+    D = 5
+    q, k, v = (RNG.standard_normal((1, 1, 1, D)) for _ in range(3))
+    o, l = oracle.attention(q, k, v, 0.3)
+    assert np.allclose(o[0, 0, 0], v[0, 0, 0], atol=1e-14)
+    assert abs(l[0, 0, 0] - 0.3 * float(q[0, 0, 0] @ k[0, 0, 0])) < 1e-13
+
+
+ATTENTION_PINS = (_pin_brute_force, _pin_torch_sdpa, _pin_zero_query, _pin_single_key)
+
+
+def _caught(pins) -> list[str]:
+    failed = []
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            failed.append(pin.__name__)
+    return failed
+
+
+# ------------------------------------------------------------------------------------------------
+# planted mistakes in the attention
+# ------------------------------------------------------------------------------------------------
+
+def _head_mutant(kind):
+    def head(q, k, v, scale, allowed):
+        Sq, D = q.shape[0], v.shape[1]
+        if k.shape[0] == 0:
+            return np.zeros((Sq, D)), np.full(Sq, NEG_INF)
+        s = (q @ k.T) if kind == "scale dropped" else scale * (q @ k.T)
+        if kind == "key index transposed" and s.shape[0] == s.shape[1]:
+            s = s.T
+        if allowed is not None and kind != "mask ignored":
+            s = np.where(allowed, s, NEG_INF)
+        m = s.max(axis=1)
+        empty = ~np.isfinite(m)
+        m_safe = np.where(empty, 0.0, m)
+        w = np.exp((m_safe[:, None] - s) if kind == "exponent sign flipped" else (s - m_safe[:, None]))
+        w = np.where(np.isfinite(w), w, 0.0)
+        l = w.sum(axis=1)
+        denom = np.where(empty, 1.0, l)[:, None]
+        out = (w @ v) if kind == "no normalisation" else (w @ v) / denom
+        if kind == "lse without the max":
+            lse = np.log(np.where(empty, 1.0, l))
+        elif kind == "lse in log2":
+            lse = m_safe + np.log2(np.where(empty, 1.0, l))
+        else:
+            lse = m_safe + np.log(np.where(empty, 1.0, l))
+        out[empty] = 0.0
+        lse[empty] = NEG_INF
+        return out, lse
+
+    return head
+
+
+HEAD_MUTANTS = ["scale dropped", "key index transposed", "mask ignored", "exponent sign flipped",
+                "no normalisation", "lse without the max", "lse in log2"]
+
+
+def test_real_oracle_passes_every_attention_pin():
+    assert _caught(ATTENTION_PINS) == []
+
+
+@pytest.mark.parametrize("kind", HEAD_MUTANTS)
+def test_attention_mutant_is_caught(kind, monkeypatch):
+    monkeypatch.setattr(ousp, "_attention_head", _head_mutant(kind))
+    assert _caught(ATTENTION_PINS), f"no pin catches: {kind}"
+
+
+def test_causal_mask_off_by_one_is_caught(monkeypatch):
+    real = ousp.attention
+
+    def strict(q, k, v, scale, causal=False, q_pos=None, k_pos=None, row_block=4096):
+        if causal:  # the planted mistake: key j visible iff pos(j) < pos(i), diagonal excluded
+            q_pos = (np.arange(q.shape[1]) if q_pos is None else np.asarray(q_pos)) - 1
+        return real(q, k, v, scale, causal, q_pos, k_pos, row_block)
+
+    monkeypatch.setattr(oracle, "attention", strict)
+    assert _caught(ATTENTION_PINS)
+
+
+# ------------------------------------------------------------------------------------------------
+# planted mistakes in the ring merge
+# ------------------------------------------------------------------------------------------------
+
+def _pin_merge_logsumexp():
+    # merging two partials of disjoint key sets gives the attention over their union
+    D = 4
+    q = RNG.standard_normal((1, 3, 1, D))
+    k, v = RNG.standard_normal((1, 10, 1, D)), RNG.standard_normal((1, 10, 1, D))
+    o1, l1 = oracle.attention(q, k[:, :4], v[:, :4], 0.5)
+    o2, l2 = oracle.attention(q, k[:, 4:], v[:, 4:], 0.5)
+    om, lm = oracle.merge(o1, l1, o2, l2)
+    of, lf = oracle.attention(q, k, v, 0.5)
+    assert np.allclose(om, of, atol=1e-13) and np.allclose(lm, lf, atol=1e-13)
+    for i in range(3):  # lse of the union = log(exp(lse_1) + exp(lse_2))
+        assert abs(math.log(math.exp(l1[0, i, 0]) + math.exp(l2[0, i, 0])) - lm[0, i, 0]) < 1e-12
+
+
+def _pin_merge_empty():
+    o = RNG.standard_normal((3, 4))
+    l = RNG.standard_normal(3)
+    om, lm = oracle.merge(o, l, np.zeros((3, 4)), np.full(3, NEG_INF))
+    assert np.array_equal(om, o) and np.array_equal(lm, l)
+
+
+MERGE_PINS = (_pin_merge_logsumexp, _pin_merge_empty)
+
+
+def _merge_mutant(kind):
+    def merge(prev_out, prev_lse, out, lse):
+        prev_out, out = np.asarray(prev_out, float), np.asarray(out, float)
+        prev_lse, lse = np.asarray(prev_lse, float), np.asarray(lse, float)
+        d = np.where(np.isfinite(prev_lse) & np.isfinite(lse), lse - prev_lse, 0.0)
+        if kind == "sigmoid argument sign":
+            d_o = -d
+        else:
+            d_o = d
+        res_out = prev_out - ousp._sigmoid(d_o)[..., None] * (prev_out - out)
+        if kind == "logsigmoid sign":
+            res_lse = prev_lse + ousp._logsigmoid(-d)
+        elif kind == "lse not combined":
+            res_lse = np.maximum(prev_lse, lse)
+        else:
+            res_lse = prev_lse - ousp._logsigmoid(-d)
+        if kind != "empty partial not skipped":
+            res_out = np.where(~np.isfinite(lse)[..., None], prev_out, res_out)
+            res_lse = np.where(~np.isfinite(lse), prev_lse, res_lse)
+        return res_out, res_lse
+    return merge
+
+
+MERGE_MUTANTS = ["sigmoid argument sign", "logsigmoid sign", "lse not combined",
+                 "empty partial not skipped"]
+
+
+def test_real_oracle_passes_every_merge_pin():
+    assert _caught(MERGE_PINS) == []
+
+
+@pytest.mark.parametrize("kind", MERGE_MUTANTS)
+def test_merge_mutant_is_caught(kind, monkeypatch):
+    monkeypatch.setattr(oracle, "merge", _merge_mutant(kind))
+    assert _caught(MERGE_PINS), f"no pin catches: {kind}"
