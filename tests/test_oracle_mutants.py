@@ -217,3 +217,132 @@ def test_real_oracle_passes_every_merge_pin():
 def test_merge_mutant_is_caught(kind, monkeypatch):
     monkeypatch.setattr(oracle, "merge", _merge_mutant(kind))
     assert _caught(MERGE_PINS), f"no pin catches: {kind}"
+
+
+# ------------------------------------------------------------------------------------------------
+# planted mistakes in the re-layout and the chunk orderings
+# ------------------------------------------------------------------------------------------------
+
+def _iota(B, S, H, D):
+    b, t, h, d = np.meshgrid(np.arange(B), np.arange(S), np.arange(H), np.arange(D), indexing="ij")
+    return ((b * 100000 + t) * 1000 + h) * 1000 + d
+
+
+def _pack(x, lens):
+    out, o = [], 0
+    for n in lens:
+        out.append(x[:, o:o + n].reshape(-1))
+        o += n
+    return np.concatenate(out)
+
+
+def _pin_textbook_reshape():
+    B, S, H, D, P = 2, 12, 6, 4, 3
+    x = _iota(B, S, H, D)
+    y = oracle.seq2head(_pack(x, [4, 4, 4]), B, H, D, [4, 4, 4])
+    view = x.reshape(B, S, P, H // P, D)
+    per = B * S * (H // P) * D
+    for p in range(P):
+        assert np.array_equal(y[p * per:(p + 1) * per].reshape(B, S, H // P, D), view[:, :, p])
+
+
+def _pin_iota_uneven():
+    B, H, D, lens, hc = 2, 5, 3, [5, 1, 7], [2, 2, 1]
+    S = sum(lens)
+    y = oracle.seq2head(_pack(_iota(B, S, H, D), lens), B, H, D, lens, hc)
+    off, ho = 0, np.concatenate([[0], np.cumsum(hc)])
+    for p in range(len(lens)):
+        blk = y[off: off + B * S * hc[p] * D].reshape(B, S, hc[p], D)
+        off += B * S * hc[p] * D
+        bb, tt, hh, dd = np.meshgrid(np.arange(B), np.arange(S), np.arange(hc[p]), np.arange(D),
+                                     indexing="ij")
+        assert np.array_equal(blk, ((bb * 100000 + tt) * 1000 + hh + ho[p]) * 1000 + dd)
+
+
+def _pin_round_trip():
+    B, H, D, lens, hc = 3, 5, 2, [5, 1, 7], [2, 2, 1]
+    src = np.random.default_rng(0).integers(0, 2**16, size=B * sum(lens) * H * D)
+    back = oracle.head2seq(oracle.seq2head(src, B, H, D, lens, hc), B, H, D, lens, hc)
+    assert np.array_equal(back, src)
+
+
+def _pin_orders():
+    zz = oracle.ring_positions("zigzag", 16, 4)
+    assert zz[0].tolist() == [0, 1, 14, 15] and zz[3].tolist() == [6, 7, 8, 9]
+    assert oracle.ring_positions("stripe", 20, 4)[1].tolist() == [1, 5, 9, 13, 17]
+    for order in ("contiguous", "zigzag", "stripe"):
+        pos = oracle.ring_positions(order, 17, 4)
+        assert np.array_equal(np.sort(np.concatenate(pos)), np.arange(17))
+
+
+LAYOUT_PINS = (_pin_textbook_reshape, _pin_iota_uneven, _pin_round_trip, _pin_orders)
+
+
+def _caught_any(pins) -> list[str]:
+    """Like _caught, but a crash (shape error, index error) also counts as caught."""
+    failed = []
+    for pin in pins:
+        try:
+            pin()
+        except Exception:  # noqa: BLE001
+            failed.append(pin.__name__)
+    return failed
+
+
+def _seq2head_mutant(kind):
+    def seq2head(src, B, H, D, seq_lens, head_counts=None):
+        P = len(seq_lens)
+        head_counts = oracle.default_split(H, P) if head_counts is None else list(head_counts)
+        so, ho = ousp._offsets(seq_lens), ousp._offsets(head_counts)
+        S = so[-1]
+        src = np.asarray(src).reshape(-1)
+        dst = np.empty(B * S * H * D, dtype=src.dtype)
+        chunks = [src[B * so[q] * H * D: B * so[q + 1] * H * D].reshape(B, seq_lens[q], H, D)
+                  for q in range(P)]
+        for p in range(P):
+            base = B * S * ho[p] * D
+            if kind == "head and sequence axes swapped":
+                Y = dst[base: base + B * S * head_counts[p] * D].reshape(B, head_counts[p], S, D)
+            else:
+                Y = dst[base: base + B * S * head_counts[p] * D].reshape(B, S, head_counts[p], D)
+            for q in range(P):
+                g = ho[p] + (1 if kind == "head offset off by one" and p > 0 else 0)
+                blk = chunks[q][:, :, g: g + head_counts[p], :]
+                if kind == "head and sequence axes swapped":
+                    Y[:, :, so[q]: so[q + 1], :] = blk.transpose(0, 2, 1, 3)
+                elif kind == "sequence offset of the next rank":
+                    o = so[(q + 1) % P]
+                    Y[:, o: o + seq_lens[q], :, :] = blk
+                else:
+                    Y[:, so[q]: so[q + 1], :, :] = blk
+        return dst
+    return seq2head
+
+
+LAYOUT_MUTANTS = ["head and sequence axes swapped", "head offset off by one",
+                  "sequence offset of the next rank"]
+
+
+def test_real_oracle_passes_every_layout_pin():
+    assert _caught_any(LAYOUT_PINS) == []
+
+
+@pytest.mark.parametrize("kind", LAYOUT_MUTANTS)
+def test_layout_mutant_is_caught(kind, monkeypatch):
+    monkeypatch.setattr(oracle, "seq2head", _seq2head_mutant(kind))
+    assert _caught_any(LAYOUT_PINS), f"no pin catches: {kind}"
+
+
+def test_zigzag_pairing_off_by_one_is_caught(monkeypatch):
+    real = ousp.ring_positions
+
+    def ring_positions(order, S, R):
+        if order != "zigzag":
+            return real(order, S, R)
+        off = ousp._offsets(oracle.default_split(S, 2 * R))  # planted: piece 2R-2-r, not 2R-1-r
+        return [np.concatenate([np.arange(off[r], off[r + 1]),
+                                np.arange(off[(2 * R - 2 - r) % (2 * R)],
+                                          off[(2 * R - 2 - r) % (2 * R) + 1])]) for r in range(R)]
+
+    monkeypatch.setattr(oracle, "ring_positions", ring_positions)
+    assert _caught_any(LAYOUT_PINS)
