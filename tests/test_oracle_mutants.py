@@ -346,3 +346,41 @@ def test_zigzag_pairing_off_by_one_is_caught(monkeypatch):
 
     monkeypatch.setattr(oracle, "ring_positions", ring_positions)
     assert _caught_any(LAYOUT_PINS)
+
+
+# ------------------------------------------------------------------------------------------------
+# planted mistakes in the whole method (chunked + merged): caught by "equals unsplit attention"
+# ------------------------------------------------------------------------------------------------
+
+def _pin_chunked_equals_unsplit():
+    # equal chunks (S = 24) first, so that a wrong mask shows as wrong values, then uneven ones
+    for S, U, R, order, causal in ((24, 1, 3, "zigzag", True), (23, 1, 3, "zigzag", True),
+                                   (23, 2, 2, "contiguous", True), (23, 1, 4, "stripe", False)):
+        q, k, v = (RNG.standard_normal((1, S, 4, 4)) for _ in range(3))
+        o, l = oracle.usp_attention(q, k, v, 0.5, causal, U, R, order)
+        ro, rl = oracle.attention(q, k, v, 0.5, causal)
+        assert np.allclose(o, ro, atol=1e-12) and np.allclose(l, rl, atol=1e-12)
+
+
+def test_real_usp_attention_passes():
+    assert _caught_any([_pin_chunked_equals_unsplit]) == []
+
+
+def test_positions_swapped_in_a_ring_step_is_caught(monkeypatch):
+    real = ousp.attention
+
+    def swapped(q, k, v, scale, causal=False, q_pos=None, k_pos=None, row_block=4096):
+        return real(q, k, v, scale, causal, k_pos if causal else q_pos,
+                    q_pos if causal else k_pos, row_block)
+
+    monkeypatch.setattr(ousp, "attention", swapped)
+    try:  # on the equal-chunk case the swap runs and must give wrong values
+        _pin_chunked_equals_unsplit()
+        raise RuntimeError("not caught")
+    except AssertionError:
+        pass
+
+
+def test_ring_partial_dropped_is_caught(monkeypatch):
+    monkeypatch.setattr(ousp, "merge", lambda po, pl, o, l: (po, pl))  # keeps only the first step
+    assert _caught_any([_pin_chunked_equals_unsplit])
