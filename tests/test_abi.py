@@ -129,3 +129,14 @@ def test_planner_counts_every_causal_pair_once(L):
             if u == 0:
                 total += int(vis.sum())
         assert total == S * (S + 1) // 2
+
+
+def test_binding_signatures_match_header(L):
+    """The ctypes argument list of every entry point has as many parameters as its declaration."""
+    text = open(os.path.join(ROOT, "include", "usp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    for name in declared_functions():
+        m = re.search(r"\b" + name + r"\s*\(([^)]*)\)\s*;", text)
+        assert m, name
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        assert len(getattr(L, name).argtypes) == len(params), name
