@@ -359,6 +359,24 @@ def cpu_oracle_sample(w, target_s: float, rng_seed: int = 0):
             f"{n} of {w.H} heads (batch 0), every query row against the full key set")
 
 
+def nvtx_ranges(torch):
+    """torch.cuda.nvtx, or do-nothing stand-ins if NVTX is unavailable (it never stops a run)."""
+    try:
+        torch.cuda.nvtx.range_push("bench")
+        torch.cuda.nvtx.range_pop()
+        return torch.cuda.nvtx
+    except Exception:  # noqa: BLE001
+        class _Off:
+            @staticmethod
+            def range_push(_name):
+                return 0
+
+            @staticmethod
+            def range_pop():
+                return 0
+        return _Off()
+
+
 def cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -472,10 +490,13 @@ def run_ours(args):
                                         w.order, o_code, stream)
 
     no_events = [None] * 5
+    nvtx = nvtx_ranges(torch)  # section ranges for profiler timelines (no-ops without a profiler)
+    nvtx.range_push("bench: warm-up")
     for _ in range(args.warmup):
         flush()
         step(handles)
     torch.cuda.synchronize()
+    nvtx.range_pop()
     if usp.usp_check_status(ws) != usp.USP_OK:
         raise RuntimeError("device status after warm-up: " + usp.lib().usp_last_error().decode())
 
@@ -490,6 +511,7 @@ def run_ours(args):
     barrier(device)
     torch.cuda.synchronize()
     clocks.mark()
+    nvtx.range_push("bench: timed steps")
     for _ in range(args.steps):
         flush()
         gpu_head_start()
@@ -499,6 +521,7 @@ def run_ours(args):
         e_finish.synchronize()
         total_ms += e_begin.elapsed_time(e_finish)
     torch.cuda.synchronize()
+    nvtx.range_pop()
     barrier(device)
     clocks.mark()
     clk = clocks.stop()
@@ -506,6 +529,7 @@ def run_ours(args):
     # per-phase breakdown (separate loop: the phase events themselves cost about 2 us each)
     phases = {"qkv_relayout": 0.0, "attention": 0.0, "merge": 0.0, "out_relayout": 0.0}
     breakdown_steps = min(args.steps, 200)
+    nvtx.range_push("bench: phase breakdown")
     for _ in range(breakdown_steps):
         flush()
         gpu_head_start()
@@ -514,6 +538,7 @@ def run_ours(args):
         t = [events[i].elapsed_time(events[i + 1]) for i in range(4)]
         for name, dt in zip(phases, t):
             phases[name] += dt
+    nvtx.range_pop()
     status = usp.usp_check_status(ws)
     if status != usp.USP_OK:
         raise RuntimeError("device status after timing: " + usp.lib().usp_last_error().decode())
@@ -521,6 +546,7 @@ def run_ours(args):
     value /= 1e12
 
     # end to end through the C ABI with host buffers
+    nvtx.range_push("bench: end to end")
     e2e_steps = max(3, min(args.steps, 50))
     o_host = torch.empty(o.shape, dtype=out_dt).pin_memory()
     l_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
@@ -583,6 +609,7 @@ def run_ours(args):
     p_end.record(s_out)  # after the last copy-out, which depends on every earlier operation
     p_end.synchronize()
     e2e_value, _ = aggregate(e2e_steps * flops, p_start.elapsed_time(p_end) / 1000.0, world, device)
+    nvtx.range_pop()
     if usp.usp_check_status(ws, s_cmp) != usp.USP_OK:
         raise RuntimeError("device status after the end-to-end loops: " +
                            usp.lib().usp_last_error().decode())
@@ -604,8 +631,10 @@ def run_ours(args):
             bw[name] = {"GB/s": gbs, "bytes": pb[name], "us": s * 1e6,
                         "frac_measured_hbm": gbs / peaks["hbm_gbs"], "frac_8TBs": gbs / NOMINAL_HBM_GBS}
     bw_bytes = sum(pb.values())
+    nvtx.range_push("bench: standalone re-layout and merge")
     standalone = standalone_relayout(w, q, k, v, o, flush, stream)
     standalone_m = standalone_merge(w, out_dt, flush, stream)
+    nvtx.range_pop()
     for part in (standalone["seq2head_qkv"], standalone["head2seq_o"], standalone_m):
         part["frac_measured_hbm"] = part["GB/s"] / peaks["hbm_gbs"]
         part["frac_8TBs"] = part["GB/s"] / NOMINAL_HBM_GBS
