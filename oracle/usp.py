@@ -15,8 +15,6 @@ Conventions, fixed once for the whole library and its oracle:
 """
 from __future__ import annotations
 
-import math
-
 import numpy as np
 
 NEG_INF = float("-inf")
@@ -335,17 +333,3 @@ def usp_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, cau
             out[:, rows] = xo[base * H * D:(base + B * rl[u]) * H * D].reshape(B, rl[u], H, D)
             lse[:, rows] = xl[base * H:(base + B * rl[u]) * H].reshape(B, rl[u], H)
     return out, lse
-
-
-def flops(B: int, H: int, D: int, S: int, causal: bool) -> float:
-    """Algorithmic attention FLOPs: 4 B H D x (number of visible query/key pairs)."""
-    pairs = S * (S + 1) // 2 if causal else S * S
-    return 4.0 * B * H * D * pairs
-
-
-def log_sum_exp(x) -> float:
-    """ln sum exp over a Python sequence (max-shifted), for small brute-force checks."""
-    m = max(x)
-    if m == NEG_INF:
-        return NEG_INF
-    return m + math.log(math.fsum(math.exp(v - m) for v in x))
