@@ -48,16 +48,17 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention TFLOP/s & % bf16 tensor peak; re-layout+merge GB/s & % HBM BW"
-DEFAULT_WORKLOAD = "flux_1024_u2"
+DEFAULT_WORKLOAD = "llm_64k_ring8_zigzag"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL_HBM_GBS = 8000.0
 
-# DRAM bytes (read + write) per launch of the partial-attention kernel from an ncu capture, with
-# the hash of the kernel sources they were taken on; reported as null once the kernel changes.
+# DRAM bytes (read + write) per launch of the attention kernel, dram__bytes_read.sum +
+# dram__bytes_write.sum from one ncu capture of that workload's launch, with the hash of the kernel
+# sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
-    # profiles/attn_fwd_flux_1024_u2.md: dram__bytes_read.sum 85.138432 MB + write 4.126464 MB
     "flux_1024_u2": {"bytes": 89264896, "kernel_hash": "15fcae45c593c630"},
 }
+L2_BYTES = 129e6
 
 
 def kernel_hash() -> str:
@@ -196,20 +197,21 @@ def workload(name: str):
     return synth.WORKLOADS[name]
 
 
-def phase_bytes(w, out_elem: int):
+def phase_bytes(w, out_elem: int, ring_mode: str):
     """Algorithmic HBM bytes of the bandwidth-bound phases (each element read once + written once).
 
     Q/K/V are re-laid by a separate pass only for zigzag order with several ring ranks whose
     half-chunks are unequal or not whole 128-row tiles (otherwise the attention's tensor maps
     address each virtual rank's head-sharded view in place); O and LSE are always written in the
-    global layout by the attention (one ring rank) or the merge."""
+    global layout by the attention (one ring rank, or fused ring steps) or by the merge (separate
+    ring steps)."""
     elems = w.B * w.S * w.H * w.D
     rows_h = w.B * w.S * w.H
     half = w.S // (2 * w.ring_degree)
     qkv_pass = (w.order == "zigzag" and w.ring_degree > 1 and
                 (w.S % (2 * w.ring_degree) != 0 or half % 128 != 0))
     b = {"qkv_relayout": 2 * 3 * elems * 2 if qkv_pass else 0}
-    if w.ring_degree > 1:
+    if ring_mode == "separate":
         # every partial's LSE is read; only partials whose rows saw a key are read in full (a
         # fully masked chunk pair leaves lse = -inf and the merge skips its O)
         seen = w.B * visible_partial_vectors(w)
@@ -258,105 +260,157 @@ class L2Flush:
         torch.sum(self.buf, 0, out=self.acc)
 
 
-def standalone_relayout(w, q, k, v, o, flush, stream, reps: int = 50):
+def back_to_back_us(launch, n_sets: int, reps: int, flush, stream):
+    """Mean device time (us) of one launch, from ``reps`` launches issued back to back between one
+    pair of events on ``stream``.  Launch i uses buffer set i mod n_sets; the sets together span
+    several times the L2, so no launch finds its inputs in L2.  A GPU spin before the first event,
+    sized from the measured host enqueue time, lets the host enqueue every launch first, so that
+    host launch latency is not timed."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(n_sets):
+        launch(i)
+    torch.cuda.synchronize()
+    head_us = 100.0 + 40.0 * reps
+    for _attempt in range(3):
+        flush()
+        gpu_head_start(head_us)
+        e0.record(stream)
+        t0 = time.perf_counter()
+        for i in range(reps):
+            launch(i % n_sets)
+        host_us = (time.perf_counter() - t0) * 1e6
+        e1.record(stream)
+        e1.synchronize()
+        if host_us < head_us:
+            break
+        head_us = 2.0 * host_us + 100.0  # the host fell behind the GPU: repeat with a longer spin
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def rotation(bytes_per_set: float) -> int:
+    """Buffer sets so that a full rotation streams at least three times the L2 (129 MB)."""
+    return max(1, math.ceil(3 * L2_BYTES / bytes_per_set))
+
+
+def standalone_relayout(w, q, k, v, o, flush, stream, reps: int = 30):
     """GB/s of the standalone Ulysses re-layout entry points on this workload's tensors: seq->head
-    of Q, K, V and head->seq of O over the Ulysses split (a separately timed measurement, since the
-    end-to-end step addresses these layouts in place)."""
+    of Q, K, V (one usp_relayout_seq2head_multi launch) and head->seq of O over the Ulysses split (a
+    separately timed measurement, since the end-to-end step addresses these layouts in place).
+    Back-to-back launches over rotating buffer sets; bytes = every element read once and written
+    once."""
     import torch
 
     from sequence_attention_tcgen05_gb300 import usp
     U = max(2, w.ulysses_degree)
     lens = [w.S // U + (1 if p < w.S % U else 0) for p in range(U)]
-    outs = [torch.empty_like(x) for x in (q, k, v)]
-    oo = torch.empty_like(o)
-    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-    t_in = t_out = 0.0
-    for i in range(reps + 3):
-        flush()
-        gpu_head_start(300.0)
-        e0.record(stream)
-        for x, y in zip((q, k, v), outs):
-            usp.usp_relayout_seq2head(x, y, w.B, w.H, w.D, lens, stream=stream)
-        e1.record(stream)
-        usp.usp_relayout_head2seq(o, oo, w.B, w.H, w.D, lens, stream=stream)
-        e2.record(stream)
-        e2.synchronize()
-        if i >= 3:
-            t_in += e0.elapsed_time(e1)
-            t_out += e1.elapsed_time(e2)
     elems = w.B * w.S * w.H * w.D
     bin_, bout = 2 * 3 * elems * 2, 2 * elems * o.element_size()
-    return {"ulysses_split": lens,
-            "seq2head_qkv": {"GB/s": bin_ / (t_in / reps / 1e3) / 1e9, "bytes": bin_,
-                             "us": t_in / reps * 1e3},
-            "head2seq_o": {"GB/s": bout / (t_out / reps / 1e3) / 1e9, "bytes": bout,
-                           "us": t_out / reps * 1e3}}
+    n_in = rotation(bin_)
+    sets_in = [((q, k, v) if i == 0 else tuple(torch.empty_like(x) for x in (q, k, v)),
+                tuple(torch.empty_like(x) for x in (q, k, v))) for i in range(n_in)]
+
+    def seq2head(i):  # Q, K and V in one launch
+        src, dst = sets_in[i]
+        usp.usp_relayout_seq2head_multi(src, dst, w.B, w.H, w.D, lens, stream=stream)
+
+    us_in = back_to_back_us(seq2head, n_in, reps, flush, stream)
+    del sets_in
+    n_out = rotation(bout)
+    sets_out = [(o if i == 0 else torch.empty_like(o), torch.empty_like(o)) for i in range(n_out)]
+
+    def head2seq(i):
+        src, dst = sets_out[i]
+        usp.usp_relayout_head2seq(src, dst, w.B, w.H, w.D, lens, stream=stream)
+
+    us_out = back_to_back_us(head2seq, n_out, reps, flush, stream)
+    del sets_out
+    return {"ulysses_split": lens, "timing": f"{reps} back-to-back launches per figure",
+            "seq2head_qkv": {"GB/s": bin_ / (us_in * 1e-6) / 1e9, "bytes": bin_, "us": us_in,
+                             "buffer_sets": n_in, "launches": 1},
+            "head2seq_o": {"GB/s": bout / (us_out * 1e-6) / 1e9, "bytes": bout, "us": us_out,
+                           "buffer_sets": n_out, "launches": 1}}
 
 
 def standalone_merge(w, out_dt, flush, stream, reps: int = 30):
     """GB/s of the standalone usp_lse_merge entry point on two fp32 ring partials of this
-    workload's size (a separately timed measurement: Ulysses-only workloads have no merge in the
-    step).  Bytes: both partials and their LSE read, O (out_dt) and LSE written."""
+    workload's size (a separately timed measurement: the step itself may have no merge).  Bytes:
+    both partials and their LSE read, O (out_dt) and LSE written.  Back-to-back launches over
+    rotating buffer sets."""
     import torch
 
     from sequence_attention_tcgen05_gb300 import usp
     rows, H, D = w.B * w.S, w.H, w.D
+    elems, rows_h = rows * H * D, rows * H
+    esz = torch.empty((), dtype=out_dt).element_size()
+    nbytes = 2 * (elems * 4 + rows_h * 4) + elems * esz + rows_h * 4
     g = torch.Generator(device="cuda").manual_seed(1)
-    o_parts = torch.randn((2, rows, H, D), dtype=torch.float32, device="cuda", generator=g)
-    l_parts = torch.randn((2, rows, H), dtype=torch.float32, device="cuda", generator=g)
-    o_out = torch.empty((rows, H, D), dtype=out_dt, device="cuda")
-    l_out = torch.empty((rows, H), dtype=torch.float32, device="cuda")
+    sets = []
+    for _ in range(rotation(nbytes)):
+        sets.append((torch.randn((2, rows, H, D), dtype=torch.float32, device="cuda", generator=g),
+                     torch.randn((2, rows, H), dtype=torch.float32, device="cuda", generator=g),
+                     torch.empty((rows, H, D), dtype=out_dt, device="cuda"),
+                     torch.empty((rows, H), dtype=torch.float32, device="cuda")))
 
-    def call():
+    def call(i):
+        o_parts, l_parts, o_out, l_out = sets[i]
         usp.usp_lse_merge(2, o_parts, rows * H * D, l_parts, rows * H, rows, H, D, o_out, l_out,
                           stream=stream)
 
-    call()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t = 0.0
-    for i in range(reps + 3):
-        flush()
-        gpu_head_start()
-        e0.record(stream)
-        call()
-        e1.record(stream)
-        e1.synchronize()
-        if i >= 3:
-            t += e0.elapsed_time(e1)
-    elems, rows_h = rows * H * D, rows * H
-    nbytes = 2 * (elems * 4 + rows_h * 4) + elems * o_out.element_size() + rows_h * 4
-    us = t / reps * 1e3
-    del o_parts, l_parts, o_out, l_out
-    return {"partials": 2, "bytes": nbytes, "us": us, "GB/s": nbytes / (us * 1e-6) / 1e9}
+    us = back_to_back_us(call, len(sets), reps, flush, stream)
+    n_sets = len(sets)
+    del sets
+    return {"partials": 2, "bytes": nbytes, "us": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
+            "buffer_sets": n_sets, "timing": f"{reps} back-to-back launches"}
 
 
-def cpu_oracle_sample(w, target_s: float, rng_seed: int = 0):
-    """Time the fp64 oracle on whole heads of the workload (all query rows of a head against its
-    full key set) until about ``target_s`` seconds have passed or every head is done; returns
-    (TFLOP/s, seconds, description of the sample)."""
+def cpu_oracle_sample(w, target_s: float, rng_seed: int = 0, max_scores: int = 1 << 26):
+    """Time the fp64 oracle on a sample of the workload: heads in a seeded random order; per head
+    every query row when the head's score matrix has at most ``max_scores`` entries, else that
+    many scores' worth of random query rows, each against the head's full key set, until about
+    ``target_s`` seconds have passed (at least one draw).  The FLOP count is the algorithmic one
+    of the sampled rows (4 D per visible query/key pair), so the rate is comparable with the GPU
+    figure.  Returns (TFLOP/s, seconds, description of the sample)."""
     import numpy as np
 
     import oracle
     from sequence_attention_tcgen05_gb300 import synth
     scale = 1.0 / math.sqrt(w.D)
-    rows = np.arange(w.S)
-    vis = (rows + 1).sum() if w.causal else w.S * w.S
-    heads = list(np.random.default_rng(rng_seed).permutation(w.H))
-    done_flops, spent, n = 0.0, 0.0, 0
+    rng = np.random.default_rng(rng_seed)
+    heads = [int(h) for h in rng.permutation(w.H)]
+    n_rows = min(w.S, max(1, max_scores // max(1, w.S)))
+    done_flops, spent, rows_done, draws = 0.0, 0.0, 0, 0
+    heads_seen = set()
     for h in heads:
-        bits = [synth.qkv_rows_bits(w.seed, st, w.B, w.S, w.H, w.D, 0, rows, int(h), w.text_rows,
-                                    w.text_scale) for st in (synth.STREAM_Q, synth.STREAM_K,
-                                                             synth.STREAM_V)]
-        q, k, v = (oracle.widen_bf16(b) for b in bits)
-        t0 = time.perf_counter()
-        oracle.attention_rows(q, k, v, scale, w.causal, rows)
-        spent += time.perf_counter() - t0
-        done_flops += 4.0 * w.D * vis
-        n += 1
+        k, v = (oracle.widen_bf16(synth.qkv_rows_bits(w.seed, st, w.B, w.S, w.H, w.D, 0,
+                                                      np.arange(w.S), h, w.text_rows,
+                                                      w.text_scale))
+                for st in (synth.STREAM_K, synth.STREAM_V))
+        heads_seen.add(h)
+        while True:  # whole head once, or random row draws of this head until the time is up
+            rows = (np.arange(w.S) if n_rows == w.S else
+                    np.sort(rng.choice(w.S, size=n_rows, replace=False)))
+            q = oracle.widen_bf16(synth.qkv_rows_bits(w.seed, synth.STREAM_Q, w.B, w.S, w.H, w.D,
+                                                      0, rows, h, w.text_rows, w.text_scale))
+            t0 = time.perf_counter()
+            oracle.attention_rows(q, k, v, scale, w.causal, rows)
+            spent += time.perf_counter() - t0
+            visible = float((rows + 1).sum()) if w.causal else float(len(rows)) * w.S
+            done_flops += 4.0 * w.D * visible
+            rows_done += len(rows)
+            draws += 1
+            if n_rows == w.S or spent >= target_s:
+                break
         if spent >= target_s:
             break
-    return (done_flops / spent / 1e12, spent,
-            f"{n} of {w.H} heads (batch 0), every query row against the full key set")
+    if n_rows == w.S:
+        desc = (f"{draws} whole heads of {w.H} (batch 0): every query row against the full key "
+                f"set")
+    else:
+        desc = (f"sampled: {rows_done} random query rows ({draws} draws of {n_rows}) of "
+                f"{len(heads_seen)} heads of {w.H} (batch 0), each against the full key set; "
+                f"FLOPs of the visible pairs only")
+    return done_flops / spent / 1e12, spent, desc
 
 
 def nvtx_ranges(torch):
@@ -435,12 +489,15 @@ def run_reference(args):
     return 0
 
 
-def config_of(w, out_dtype: str):
-    return {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D,
-            "ulysses_degree": w.ulysses_degree, "ring_degree": w.ring_degree,
-            "causal": w.causal, "order": w.order, "text_rows": w.text_rows,
-            "seq_lens": list(w.seq_lens) or "default split", "out_dtype": out_dtype,
-            "l2": "flushed between timed steps (256 MiB read outside the step events)"}
+def config_of(w, out_dtype: str, ring_mode: str | None = None):
+    c = {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D,
+         "ulysses_degree": w.ulysses_degree, "ring_degree": w.ring_degree,
+         "causal": w.causal, "order": w.order, "text_rows": w.text_rows,
+         "seq_lens": list(w.seq_lens) or "default split", "out_dtype": out_dtype,
+         "l2": "flushed between timed steps (256 MiB read outside the step events)"}
+    if ring_mode is not None:
+        c["ring_steps"] = ring_mode
+    return c
 
 
 def run_ours(args):
@@ -469,7 +526,9 @@ def run_ours(args):
     o = torch.empty((B, S, H, D), dtype=out_dt, device=device)
     lse = torch.empty((B, S, H), dtype=torch.float32, device=device)
     nbytes = usp.usp_attention_workspace_size(B, S, H, D, w.ulysses_degree, w.ring_degree,
-                                              w.order, o_code)
+                                              w.order, o_code, w.causal)
+    ring_mode = usp.usp_attention_ring_mode(B, S, H, D, w.causal, w.ulysses_degree, w.ring_degree,
+                                            w.order, o_code)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
     flush = L2Flush(device)  # 256 MiB > L2
     stream = torch.cuda.current_stream()
@@ -491,6 +550,10 @@ def run_ours(args):
 
     no_events = [None] * 5
     nvtx = nvtx_ranges(torch)  # section ranges for profiler timelines (no-ops without a profiler)
+    # clocks are sampled from before the warm-up, so that the GPU goes straight from the warm-up
+    # steps into the timed ones (no idle gap that would let it cool and change clocks)
+    clocks = ClockSampler(local)
+    clocks.start()
     nvtx.range_push("bench: warm-up")
     for _ in range(args.warmup):
         flush()
@@ -502,11 +565,9 @@ def run_ours(args):
 
     # headline: one event pair around each step; the flush and a short GPU spin before the start
     # event let the host enqueue the whole step before the GPU reaches it
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
     e_begin, e_finish = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     total_ms = 0.0
+    step_ms = []
     launches = 0
     barrier(device)
     torch.cuda.synchronize()
@@ -516,10 +577,11 @@ def run_ours(args):
         flush()
         gpu_head_start()
         e_begin.record(stream)
-        launches += step(no_events)
+        launches += sum(step(no_events))
         e_finish.record(stream)
         e_finish.synchronize()
-        total_ms += e_begin.elapsed_time(e_finish)
+        step_ms.append(e_begin.elapsed_time(e_finish))
+        total_ms += step_ms[-1]
     torch.cuda.synchronize()
     nvtx.range_pop()
     barrier(device)
@@ -528,12 +590,13 @@ def run_ours(args):
 
     # per-phase breakdown (separate loop: the phase events themselves cost about 2 us each)
     phases = {"qkv_relayout": 0.0, "attention": 0.0, "merge": 0.0, "out_relayout": 0.0}
+    phase_launches = [0, 0, 0, 0]
     breakdown_steps = min(args.steps, 200)
     nvtx.range_push("bench: phase breakdown")
     for _ in range(breakdown_steps):
         flush()
         gpu_head_start()
-        step(handles)
+        phase_launches = step(handles)
         events[4].synchronize()
         t = [events[i].elapsed_time(events[i + 1]) for i in range(4)]
         for name, dt in zip(phases, t):
@@ -544,6 +607,27 @@ def run_ours(args):
         raise RuntimeError("device status after timing: " + usp.lib().usp_last_error().decode())
     value, t_max = aggregate(args.steps * flops, total_ms / 1000.0, world, device)
     value /= 1e12
+
+    # the same step on a QKV-packed input [B][S][3][H][D] (usp_attention_qkvpacked), timed the
+    # same way over a shorter loop
+    nvtx.range_push("bench: packed QKV")
+    qkv = torch.stack([q, k, v], dim=2).contiguous()
+    packed_steps = min(args.steps, 50)
+    packed_ms = 0.0
+    for i in range(packed_steps + 3):
+        flush()
+        gpu_head_start()
+        e_begin.record(stream)
+        usp.usp_attention_qkvpacked(qkv, B, S, H, D, scale, w.causal, w.ulysses_degree,
+                                    w.ring_degree, o, lse, ws, nbytes, seq, None, w.order, o_code,
+                                    stream)
+        e_finish.record(stream)
+        e_finish.synchronize()
+        if i >= 3:
+            packed_ms += e_begin.elapsed_time(e_finish)
+    del qkv
+    nvtx.range_pop()
+    packed_value, _ = aggregate(packed_steps * flops, packed_ms / 1000.0, world, device)
 
     # end to end through the C ABI with host buffers
     nvtx.range_push("bench: end to end")
@@ -622,15 +706,16 @@ def run_ours(args):
     peak = peaks["bf16_tflops"]
     traffic = ATTN_TRAFFIC.get(w.name)
     traffic_bytes = traffic["bytes"] if traffic and traffic["kernel_hash"] == kernel_hash() else None
-    pb = phase_bytes(w, out_elem)
+    pb = phase_bytes(w, out_elem, ring_mode)
+    ran = dict(zip(phases, (n > 0 for n in phase_launches)))
     bw = {}
     for name in ("qkv_relayout", "merge"):
-        if pb[name]:
+        if pb[name] and ran[name]:
             s = phases[name] / 1000.0 / breakdown_steps
             gbs = pb[name] / s / 1e9
             bw[name] = {"GB/s": gbs, "bytes": pb[name], "us": s * 1e6,
                         "frac_measured_hbm": gbs / peaks["hbm_gbs"], "frac_8TBs": gbs / NOMINAL_HBM_GBS}
-    bw_bytes = sum(pb.values())
+    bw_bytes = sum(pb[n] for n in ("qkv_relayout", "merge") if ran[n])
     nvtx.range_push("bench: standalone re-layout and merge")
     standalone = standalone_relayout(w, q, k, v, o, flush, stream)
     standalone_m = standalone_merge(w, out_dt, flush, stream)
@@ -638,16 +723,18 @@ def run_ours(args):
     for part in (standalone["seq2head_qkv"], standalone["head2seq_o"], standalone_m):
         part["frac_measured_hbm"] = part["GB/s"] / peaks["hbm_gbs"]
         part["frac_8TBs"] = part["GB/s"] / NOMINAL_HBM_GBS
-    bw_s = sum(phases[n] for n in ("qkv_relayout", "merge")) / 1000.0 / breakdown_steps
+    bw_s = sum(phases[n] for n in ("qkv_relayout", "merge") if ran[n]) / 1000.0 / breakdown_steps
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_max * 1000.0 / args.steps, "higher_is_better": True,
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
+                    "max": max(step_ms)},
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, args.out_dtype),
+        "config": config_of(w, args.out_dtype, ring_mode),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic_bytes,
-                     "kernel": "attn_fwd_kernel (partial attention, all chunk pairs, one launch)",
+                     "kernel": "attn_fwd_kernel (all chunk pairs and ring steps, one launch)",
                      "peak_kind": f"{peak_kind} bf16 burst",
                      "frac_sustained_peak": achieved / peaks["bf16_tflops_sustained"]},
         "relayout_merge": {"GB/s": bw_bytes / bw_s / 1e9 if bw_s > 0 else None,
@@ -655,13 +742,18 @@ def run_ours(args):
                            "frac_8TBs": (bw_bytes / bw_s / 1e9 / NOMINAL_HBM_GBS) if bw_s > 0 else None,
                            "phases": bw, "standalone_relayout": standalone,
                            "standalone_merge": standalone_m},
-        "phases_ms_per_step": {k: v / breakdown_steps for k, v in phases.items()},
+        "phases_ms_per_step": {k: (v / breakdown_steps if ran[k] else None)
+                               for k, v in phases.items()},
+        "phase_launches": dict(zip(phases, phase_launches)),
         "phases_steps": breakdown_steps,
         "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "mode": "pipelined: step i's copy-in overlaps step i-1's attention and copy-out "
                         "(two device buffer sets, one stream per link direction)",
                 "serial_value": e2e_serial / 1e12},
+        "qkvpacked": {"value": packed_value / 1e12, "unit": "TFLOP/s",
+                      "ms_per_step": packed_ms / packed_steps, "steps": packed_steps,
+                      "input": "bf16 [B][S][3][H][D] through usp_attention_qkvpacked"},
         "gpu_launches": launches,
         "clocks": clk,
     }

@@ -103,6 +103,21 @@ usp_status_t usp_relayout_head2seq(const void* src, void* dst, usp_dtype_t dt, i
                                    int P, const int32_t* seq_lens, const int32_t* head_counts,
                                    usp_stream_t stream);
 
+/* The same two re-layouts for n_tensors (1..3) tensors of one shape in ONE launch — Q, K and V
+ * before the attention ([CP] Ulysses Attention: the first all-to-all moves the query, key and
+ * value projections), or O and a second output after it.  src and dst are HOST arrays of
+ * n_tensors device pointers, read during the call; tensor t moves from src[t] to dst[t] exactly
+ * as in usp_relayout_seq2head / usp_relayout_head2seq.  Errors: as those, plus INVALID_ARG for
+ * n_tensors outside [1, 3] or a NULL entry. */
+usp_status_t usp_relayout_seq2head_multi(int n_tensors, const void* const* src, void* const* dst,
+                                         usp_dtype_t dt, int B, int H, int D, int P,
+                                         const int32_t* seq_lens, const int32_t* head_counts,
+                                         usp_stream_t stream);
+usp_status_t usp_relayout_head2seq_multi(int n_tensors, const void* const* src, void* const* dst,
+                                         usp_dtype_t dt, int B, int H, int D, int P,
+                                         const int32_t* seq_lens, const int32_t* head_counts,
+                                         usp_stream_t stream);
+
 /* usp_reorder — global sequence <-> ring-rank chunks under an ordering [YC].
  *   inverse = 0: src is global [B][S][H][D]; dst is R chunks back to back, chunk r is
  *                [B][s_r][H][D] holding rank r's tokens in local order (see usp_order_t).
@@ -139,8 +154,9 @@ usp_status_t usp_attn_partial(const void* q, const void* k, const void* v, int B
  * lse = prev_lse - logsigmoid(prev_lse - lse), in fp32).  This kernel merges all partials of a
  * row in one pass with the equivalent max-shifted form (exact in real arithmetic):
  * m = max_k lse_k, w_k = exp(lse_k - m), out = sum_k w_k out_k / sum_k w_k,
- * lse = m + ln sum_k w_k.  Partials with lse = -inf contribute nothing and their out is not read;
- * a row whose partials are all -inf gets out = 0, lse = -inf.
+ * lse = m + ln sum_k w_k.  Partials with lse = -inf contribute nothing: their out is loaded
+ * with the LSE but never used, so it may hold any bits (NaN included) as long as the memory is
+ * readable; a row whose partials are all -inf gets out = 0, lse = -inf.
  *
  *   o_parts: fp32, part k at o_parts + k*o_part_stride (elements), each [n_rows][H][D].
  *   lse_parts: fp32, part k at lse_parts + k*lse_part_stride, each [n_rows][H].
@@ -172,10 +188,20 @@ usp_status_t usp_lse_merge(int n_parts, const float* o_parts, int64_t o_part_str
  *   run of global rows (contiguous or stripe order, one ring rank) or, under zigzag, two equal
  *   half-chunks of whole 128-row tiles (S divisible by 256 * ring_degree); otherwise a fused
  *   reorder + seq->head pass copies Q, K, V into the workspace first.
- *   (2) One partial-attention launch over every (ring step, chunk pair, head, query block), with
- *   fully masked causal tiles skipped.  (3) With several ring ranks, the LSE merge of the ring
- *   partials.  The head->seq re-layout and inverse reorder of O and LSE are the store addressing
- *   of (2) (one ring rank) or (3): the result lands in the global layout directly.
+ *   (2) One attention launch over every (ring step, chunk pair, head, query block), with fully
+ *   masked causal tiles skipped.  With several ring ranks the ring steps are either
+ *     - fused: each 256-row query block carries one online softmax across the visible K/V chunks
+ *       of all ring steps, in ring order ([CP] Ring Attention: K/V blocks pass around the ring;
+ *       the running (max, sum, output) is the LSE-weighted merge of [USP] done in registers),
+ *       and writes the final O and LSE; or
+ *     - separate: every ring step writes an fp32 partial (O, LSE) into the workspace and
+ *       (3) an LSE merge pass combines them.
+ *   The library picks the mode with the shorter modelled time (the merge pass and per-step
+ *   epilogues against the load balance of fewer, longer units); the choice depends only on the
+ *   arguments, so usp_attention_workspace_size and usp_attention agree.  USP_RING_MERGE=fused or
+ *   =separate in the environment (read at each call) overrides it.  The head->seq re-layout and
+ *   inverse reorder of O and LSE are the store addressing of (2) (one ring rank, or fused) or
+ *   (3): the result lands in the global layout directly.
  *   Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA as above. */
 usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
                            float scale, int causal, int ulysses_degree, int ring_degree,
@@ -183,19 +209,35 @@ usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, i
                            void* o, usp_dtype_t o_dt, float* lse, void* workspace,
                            size_t workspace_bytes, usp_stream_t stream);
 
+/* usp_attention on a QKV-packed input ([YC]: yunchang ships QKV-packed variants of its
+ * attention functions, which outperform the unpacked ones): qkv is bf16 [B][S][3][H][D], i.e.
+ * token t of batch b holds its query heads, then its key heads, then its value heads, in one row
+ * of 3*H*D elements (the layout a fused QKV projection writes).  The attention's tensor maps read
+ * the three tensors in place with a 3*H*D row stride, so nothing is unpacked; where usp_attention
+ * copies Q, K, V into the workspace (zigzag chunks whose half-chunks are not whole 128-row tiles)
+ * the copy reads the packed rows directly.  All other arguments, outputs, workspace and errors are
+ * those of usp_attention (qkv must be 16-byte aligned). */
+usp_status_t usp_attention_qkvpacked(const void* qkv, int B, int S, int H, int D, float scale,
+                                     int causal, int ulysses_degree, int ring_degree,
+                                     const int32_t* seq_lens, const int32_t* head_counts,
+                                     usp_order_t order, void* o, usp_dtype_t o_dt, float* lse,
+                                     void* workspace, size_t workspace_bytes,
+                                     usp_stream_t stream);
+
 /* usp_attention with phase timing: identical work, and additionally records the caller's CUDA
  * events (cudaEvent_t handles, created by the caller) on `stream`:
  *   events[0] before the first launch, events[1] after the Q/K/V re-layout, events[2] after the
  *   partial-attention launch(es), events[3] after the merge, events[4] after the output
  *   re-layout.  A skipped phase records its event at the same point as the previous one.
- *   `events` must hold 5 handles (entries may be NULL to skip a record).  If `n_launches` is not
- *   NULL it receives the number of kernels launched.  Errors as usp_attention. */
+ *   `events` must hold 5 handles (entries may be NULL to skip a record).  If `launches` is not
+ *   NULL it receives 4 counts: kernels launched for the Q/K/V re-layout, the attention, the merge
+ *   and the output re-layout (0 for a phase that did not run).  Errors as usp_attention. */
 usp_status_t usp_attention_events(const void* q, const void* k, const void* v, int B, int S, int H,
                                   int D, float scale, int causal, int ulysses_degree,
                                   int ring_degree, const int32_t* seq_lens,
                                   const int32_t* head_counts, usp_order_t order, void* o,
                                   usp_dtype_t o_dt, float* lse, void* workspace,
-                                  size_t workspace_bytes, void* const* events, int* n_launches,
+                                  size_t workspace_bytes, void* const* events, int* launches,
                                   usp_stream_t stream);
 
 /* usp_attention_noalloc — usp_attention without a workspace, for callers that cannot allocate
@@ -209,12 +251,15 @@ usp_status_t usp_attention_events(const void* q, const void* k, const void* v, i
  *   usp_attention_workspace_size exceeds 128 MiB are rejected with USP_ERR_WORKSPACE and a message
  *   giving both sizes; nothing is launched then.
  *   The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- *   with that device current) and caches it; make that first call before any stream capture.
+ *   with that device current) and caches it with the device's current CUDA context; make that
+ *   first call before any stream capture.  If the context changes (after cudaDeviceReset the
+ *   library's module is loaded again), the next call looks the address up again.
  *   Every call shares the array and finds the previous call's data in it; each call clears the
  *   status word it needs zeroed.  Calls that overlap on the GPU (several streams or host threads
  *   on one device) race on the array: serialise them.
  *   status: optional device uint32 that receives this call's bounded-wait status word (pass it to
- *   usp_check_status), or NULL.
+ *   usp_check_status).  With status = NULL a timed-out wait is not reported: the array's own
+ *   status word is cleared by the next call and has no address the caller can read.
  *   This entry point calls no cudaMalloc or cudaFree and no allocating library routine. */
 usp_status_t usp_attention_noalloc(const void* q, const void* k, const void* v, int B, int S, int H,
                                    int D, float scale, int causal, int ulysses_degree,
@@ -223,9 +268,18 @@ usp_status_t usp_attention_noalloc(const void* q, const void* k, const void* v, 
                                    usp_dtype_t o_dt, float* lse, uint32_t* status,
                                    usp_stream_t stream);
 
-/* Bytes of workspace usp_attention needs for these arguments (0 on invalid arguments). */
-size_t usp_attention_workspace_size(int B, int S, int H, int D, int ulysses_degree,
+/* Bytes of workspace usp_attention needs for these arguments (0 on invalid arguments): a 256-byte
+ * status word, plus Q, K, V copies when they cannot be addressed in place, plus ring_degree fp32
+ * partial slots of O and LSE when the ring steps run separately (see usp_attention). */
+size_t usp_attention_workspace_size(int B, int S, int H, int D, int causal, int ulysses_degree,
                                     int ring_degree, usp_order_t order, usp_dtype_t o_dt);
+
+/* Host-only query (no device needed): how usp_attention runs the ring steps for these arguments.
+ * Returns 0 with one ring rank, 1 when every ring step writes an fp32 partial and a merge pass
+ * combines them, 2 when the ring steps are fused into one online softmax per query block (see
+ * usp_attention), or -1 on invalid arguments (usp_last_error says why). */
+int usp_attention_ring_mode(int B, int S, int H, int D, int causal, int ulysses_degree,
+                            int ring_degree, usp_order_t order, usp_dtype_t o_dt);
 
 /* Synchronises `stream`, reads the device status word at `status` (a usp_attention workspace or
  * the uint32 given to usp_attn_partial), clears it, and returns USP_ERR_TIMEOUT if a bounded wait

@@ -6,6 +6,8 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <memory>
+#include <mutex>
 #include <string>
 
 #include "internal.h"
@@ -63,6 +65,25 @@ usp_status_t check_device() {
     return fail(USP_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
                 major, minor);
   return USP_OK;
+}
+
+int sm_count() {
+  constexpr int kMaxDev = 64;
+  static int cached[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (cached[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 std::vector<int> default_split(int n, int P) {
@@ -192,6 +213,11 @@ bool two_pieces(const Positions& ps) {
 
 struct Grid {
   int B = 0, S = 0, H = 0, D = 0, U = 0, R = 0;
+  bool causal = false;
+  // Ring mode (several ring ranks): fused = each query block's online softmax runs across the K/V
+  // chunks of every ring step and writes the final O and LSE (the merge happens in registers);
+  // otherwise every ring step writes an fp32 partial and a merge pass combines them.
+  bool fused_ring = false;
   usp_order_t order = USP_ORDER_CONTIGUOUS;
   std::vector<Positions> pos;  // per ring group
   std::vector<int> S_r;        // ring chunk lengths
@@ -211,8 +237,11 @@ struct Grid {
   }
 };
 
-usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int U, int R, usp_order_t order,
-                        const int32_t* seq_lens, const int32_t* head_counts, usp_dtype_t o_dt) {
+bool choose_fused_ring(const Grid& g, usp_dtype_t o_dt);
+
+usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int causal, int U, int R,
+                        usp_order_t order, const int32_t* seq_lens, const int32_t* head_counts,
+                        usp_dtype_t o_dt) {
   if (B < 1 || S < 0 || H < 1) return fail(USP_ERR_INVALID_ARG, "need B >= 1, S >= 0, H >= 1");
   if (D != 64 && D != 128) return fail(USP_ERR_UNSUPPORTED, "head dim D=%d: only 64 and 128 are built", D);
   if (U < 1 || R < 1 || U > 16 || R > 16 || U * R > 16)
@@ -222,6 +251,7 @@ usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int U, int R, usp_o
   if (o_dt != USP_BF16 && o_dt != USP_FP32) return fail(USP_ERR_INVALID_ARG, "o_dt must be BF16 or FP32");
   if (int64_t(B) * S * H * D >= (int64_t(1) << 40)) return fail(USP_ERR_INVALID_ARG, "tensor too large");
   g.B = B; g.S = S; g.H = H; g.D = D; g.U = U; g.R = R; g.order = order;
+  g.causal = causal != 0;
   g.pos = ring_positions(order, S, R);
   g.S_r.resize(R);
   for (int r = 0; r < R; ++r) g.S_r[r] = g.pos[r].rows();
@@ -271,7 +301,8 @@ usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int U, int R, usp_o
     g.off_k = take(g.elems * 2);
     g.off_v = take(g.elems * 2);
   }
-  if (R > 1) {
+  g.fused_ring = R > 1 && choose_fused_ring(g, o_dt);
+  if (R > 1 && !g.fused_ring) {
     g.off_opart = take(size_t(R) * g.elems * 4);
     g.off_lpart = take(size_t(R) * rowsH * 4);
   }
@@ -279,10 +310,275 @@ usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int U, int R, usp_o
   return USP_OK;
 }
 
+// ------------------------------------------------------------------------------------------------
+// Attention work lists.  Output placement of a segment: ring partial slot k of block (r, u) (the W
+// layout, fp32), or the final global [B][S][H] layout through ring chunk r's positions.
+// ------------------------------------------------------------------------------------------------
+// Where a segment writes: byte offsets from the caller's o and lse (the final output), or from the
+// workspace (a ring partial slot).  Plans hold offsets, not pointers, so that they can be reused
+// across calls with other buffers.
+struct SegOut {
+  bool partial;
+  int64_t o_off, lse_off;  // bytes
+};
+
+struct AttnPlan {
+  std::vector<AttnSeg> segs;  // o and lse are filled in per call from `outs`
+  std::vector<SegOut> outs;
+  std::vector<AttnLink> links;
+};
+
+int map_index(const Grid& g, int r, int u, int t) { return (r * g.U + u) * 3 + t; }
+
+SegOut set_final_output(AttnSeg& s, const Grid& g, int r, int u, int oel) {
+  s.o_bstride = g.S; s.o_heads = g.H;
+  s.o_start0 = g.pos[r].start[0]; s.o_len0 = g.pos[r].n_seg > 1 ? g.pos[r].len[0] : INT_MAX;
+  s.o_start1 = g.pos[r].start[1]; s.o_stride = g.pos[r].stride;
+  return {false, int64_t(g.hoff[u]) * g.D * oel, int64_t(g.hoff[u]) * 4};
+}
+
+// A zigzag chunk addressed in place is two maps' worth of pieces: every run must start on a
+// 128-row tile so that no tile straddles its half-chunks (runs start at 0 or at the second half
+// for these orderings).
+usp_status_t check_run_start(const Grid& g, int r, const Run& run) {
+  if (g.fused_in && two_pieces(g.pos[r]) && run.q0 % kAttnBM != 0)
+    return fail(USP_ERR_UNSUPPORTED, "zigzag run at row %d does not start on a 128-row tile", run.q0);
+  return USP_OK;
+}
+
+// One segment per (ring rank r, ring step k, Ulysses rank u, run of query rows), one link each.
+usp_status_t plan_separate(const Grid& g, int oel, AttnPlan& pl) {
+  const int64_t slot_o = g.elems * 4, slot_l = int64_t(g.B) * g.S * g.H;
+  for (int r = 0; r < g.R; ++r) {
+    for (int kstep = 0; kstep < g.R; ++kstep) {
+      const int r2 = (r - kstep + g.R) % g.R;
+      const std::vector<Run> runs = plan_runs(g.pos[r], g.pos[r2], g.causal);
+      for (const Run& run : runs)
+        if (usp_status_t st = check_run_start(g, r, run)) return st;
+      for (int u = 0; u < g.U; ++u) {
+        for (const Run& run : runs) {
+          AttnSeg s{};
+          s.q_map = map_index(g, r, u, 0);
+          s.q_row0 = run.q0; s.q_len = run.q_len;
+          s.link0 = static_cast<int>(pl.links.size()); s.n_links = 1;
+          pl.links.push_back({map_index(g, r2, u, 1), map_index(g, r2, u, 2), 0, run.kv_len, run.diag});
+          s.n_heads = g.h[u];
+          s.grp = u;
+          s.o_row0 = run.q0;
+          s.rev = g.causal;
+          if (g.R > 1) {
+            pl.outs.push_back({true, int64_t(g.off_opart) + kstep * slot_o + g.woff(r, u, g.D) * 4,
+                               int64_t(g.off_lpart) + (kstep * slot_l + g.woff(r, u, 1)) * 4});
+            s.o_bstride = g.S_r[r]; s.o_heads = g.h[u];
+            s.o_start0 = 0; s.o_len0 = INT_MAX; s.o_start1 = 0; s.o_stride = 1;
+          } else {
+            pl.outs.push_back(set_final_output(s, g, r, u, oel));
+          }
+          pl.segs.push_back(s);
+        }
+      }
+    }
+  }
+  return USP_OK;
+}
+
+// Ring steps fused: the query rows of ring chunk r are cut at every run boundary of every ring
+// step, so that within a piece each step's visible keys keep the run form (clamp(i + e, 0, L));
+// a piece is one segment whose links are the ring steps k = 0..R-1 in ring order (K/V chunk
+// (r - k) mod R), skipping steps that no row of the piece sees.
+usp_status_t plan_fused(const Grid& g, int oel, AttnPlan& pl) {
+  for (int r = 0; r < g.R; ++r) {
+    const int Sr = g.S_r[r];
+    if (Sr == 0) continue;
+    std::vector<std::vector<Run>> runs(g.R);
+    std::vector<int> cuts = {0, Sr};
+    for (int kstep = 0; kstep < g.R; ++kstep) {
+      runs[kstep] = plan_runs(g.pos[r], g.pos[(r - kstep + g.R) % g.R], g.causal);
+      for (const Run& run : runs[kstep]) {
+        if (usp_status_t st = check_run_start(g, r, run)) return st;
+        cuts.push_back(run.q0);
+      }
+    }
+    std::sort(cuts.begin(), cuts.end());
+    cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
+    for (size_t ci = 0; ci + 1 < cuts.size(); ++ci) {
+      const int a = cuts[ci], b = cuts[ci + 1];
+      for (int u = 0; u < g.U; ++u) {
+        AttnSeg s{};
+        s.q_map = map_index(g, r, u, 0);
+        s.q_row0 = a; s.q_len = b - a;
+        s.link0 = static_cast<int>(pl.links.size());
+        for (int kstep = 0; kstep < g.R; ++kstep) {
+          const int r2 = (r - kstep + g.R) % g.R;
+          const Run* run = nullptr;
+          for (const Run& x : runs[kstep])
+            if (x.q0 <= a && a < x.q0 + x.q_len) run = &x;
+          if (!run || run->kv_len == 0) continue;
+          const int diag = run->diag == kNoDiag ? kNoDiag : run->diag + (a - run->q0);
+          if (diag != kNoDiag && (b - a - 1) + diag < 0) continue;  // no row of the piece sees a key
+          pl.links.push_back({map_index(g, r2, u, 1), map_index(g, r2, u, 2), 0, run->kv_len, diag});
+        }
+        s.n_links = static_cast<int>(pl.links.size()) - s.link0;
+        s.n_heads = g.h[u];
+        s.grp = u;
+        s.o_row0 = a;
+        s.rev = g.causal;
+        pl.outs.push_back(set_final_output(s, g, r, u, oel));
+        pl.segs.push_back(s);
+      }
+    }
+  }
+  return USP_OK;
+}
+
+// Modelled time of one launch in key-tile periods: units dealt as the kernel deals them (per unit
+// group, head-major over the group's segments taken longest first; snake order over the CTAs),
+// each costing its key tiles plus an epilogue overhead.
+double launch_periods(std::vector<AttnSeg> segs, const std::vector<AttnLink>& links, int B,
+                      double overhead, int ctas) {
+  auto seg_cost = [&](const AttnSeg& s) {
+    long long c = 0;
+    for (int i = 0; i < s.n_links; ++i) c += link_tiles(links[s.link0 + i], s.q_len - 1);
+    return c;
+  };
+  std::stable_sort(segs.begin(), segs.end(), [&](const AttnSeg& a, const AttnSeg& b) {
+    return a.grp != b.grp ? a.grp < b.grp : seg_cost(a) > seg_cost(b);
+  });
+  std::vector<double> load(ctas, 0.0);
+  long long unit = 0;
+  size_t g0 = 0;
+  while (g0 < segs.size()) {
+    size_t g1 = g0;
+    while (g1 < segs.size() && segs[g1].grp == segs[g0].grp) ++g1;
+    std::vector<int> tiles;  // the group's blocks in visiting order, per (batch, head)
+    for (size_t i = g0; i < g1; ++i) {
+      const AttnSeg& s = segs[i];
+      const int n_qblk = (s.q_len + kAttnUnitRows - 1) / kAttnUnitRows;
+      for (int qi = 0; qi < n_qblk; ++qi) {
+        const int qb = s.rev ? n_qblk - 1 - qi : qi;
+        const int last = std::min(s.q_len, (qb + 1) * kAttnUnitRows) - 1;
+        int n = 0;
+        for (int l = 0; l < s.n_links; ++l) n += link_tiles(links[s.link0 + l], last);
+        tiles.push_back(n);
+      }
+    }
+    for (long long hb = 0; hb < int64_t(segs[g0].n_heads) * B; ++hb) {
+      for (int n : tiles) {
+        const long long t = unit / ctas, c = unit % ctas;
+        load[(t & 1) ? ctas - 1 - c : c] += n + overhead;
+        ++unit;
+      }
+    }
+    g0 = g1;
+  }
+  return *std::max_element(load.begin(), load.end());
+}
+
+// Fused or separate ring steps, from the modelled time of both: the separate mode also pays its
+// merge pass (bytes at about 6 TB/s; one key-tile period is about 1.55 us) and a larger epilogue
+// per unit (fp32 partial rows).  The same arguments always give the same answer (no device
+// query), so usp_attention_workspace_size and usp_attention agree.  USP_RING_MERGE=fused or
+// =separate (environment, read at each call) overrides the model.
+bool choose_fused_ring(const Grid& g, usp_dtype_t o_dt) {
+  const char* env = std::getenv("USP_RING_MERGE");
+  if (env && std::strcmp(env, "fused") == 0) return true;
+  if (env && std::strcmp(env, "separate") == 0) return false;
+  constexpr int kModelCtas = 152;
+  constexpr double kPeriodBytes = 6.0e12 * 1.55e-6;  // merge bytes per key-tile period
+  AttnPlan sep, fus;
+  if (plan_separate(g, 4, sep) != USP_OK) return false;
+  if (plan_fused(g, 4, fus) != USP_OK) return false;
+  const double t_sep = launch_periods(sep.segs, sep.links, g.B, 2.5, kModelCtas);
+  const double t_fus = launch_periods(fus.segs, fus.links, g.B, o_dt == USP_BF16 ? 2.0 : 2.5, kModelCtas);
+  // merge bytes: every partial LSE, the O of partials whose rows saw a key, the final O and LSE
+  double seen_vec = 0;
+  for (const AttnSeg& s : sep.segs) {
+    const AttnLink& lk = sep.links[s.link0];
+    if (lk.kv_len == 0) continue;
+    const int rows = lk.diag == kNoDiag ? s.q_len : std::max(0, s.q_len - std::max(0, -lk.diag));
+    seen_vec += double(rows) * s.n_heads * g.B;
+  }
+  const double rows_h = double(g.B) * g.S * g.H;
+  const double merge_bytes = g.R * rows_h * 4 + seen_vec * g.D * 4 +
+                             rows_h * (g.D * (o_dt == USP_BF16 ? 2 : 4) + 4);
+  return t_fus <= t_sep + merge_bytes / kPeriodBytes;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Plan cache.  Planning a long ring (the chunk-pair runs of every ring step, the ring-mode time
+// model) takes milliseconds on the host; a caller running the same shapes step after step gets
+// the plan from here, and each call only binds its buffers and encodes its tensor maps.  Keyed by
+// every argument that shapes the plan (and the USP_RING_MERGE override); the last kPlanCache
+// plans are kept.
+// ------------------------------------------------------------------------------------------------
+struct PlanKey {
+  int B, S, H, D, causal, U, R, order, o_dt, ring_env;
+  std::vector<int32_t> seq_lens, head_counts;
+  bool operator==(const PlanKey& o) const {
+    return B == o.B && S == o.S && H == o.H && D == o.D && causal == o.causal && U == o.U &&
+           R == o.R && order == o.order && o_dt == o.o_dt && ring_env == o.ring_env &&
+           seq_lens == o.seq_lens && head_counts == o.head_counts;
+  }
+};
+
+struct PlanEntry {
+  PlanKey key;
+  Grid g;
+  AttnPlan plan;
+};
+
+constexpr size_t kPlanCache = 16;
+std::mutex g_plan_mu;
+std::vector<std::shared_ptr<const PlanEntry>> g_plan_cache;  // most recent first
+
+int ring_env() {
+  const char* env = std::getenv("USP_RING_MERGE");
+  if (env && std::strcmp(env, "fused") == 0) return 1;
+  if (env && std::strcmp(env, "separate") == 0) return 2;
+  return 0;
+}
+
+// The validated grid and attention plan for these arguments (built and cached on first use).
+usp_status_t get_plan(int B, int S, int H, int D, int causal, int U, int R, usp_order_t order,
+                      const int32_t* seq_lens, const int32_t* head_counts, usp_dtype_t o_dt,
+                      std::shared_ptr<const PlanEntry>& out) {
+  PlanKey key{B, S, H, D, causal != 0, U, R, static_cast<int>(order), static_cast<int>(o_dt), ring_env(), {}, {}};
+  if (seq_lens && U >= 1 && R >= 1 && U <= 16 && R <= 16) key.seq_lens.assign(seq_lens, seq_lens + U * R);
+  if (head_counts && U >= 1 && U <= 16) key.head_counts.assign(head_counts, head_counts + U);
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    for (size_t i = 0; i < g_plan_cache.size(); ++i) {
+      if (g_plan_cache[i]->key == key) {
+        out = g_plan_cache[i];
+        if (i > 0) {
+          g_plan_cache.erase(g_plan_cache.begin() + i);
+          g_plan_cache.insert(g_plan_cache.begin(), out);
+        }
+        return USP_OK;
+      }
+    }
+  }
+  auto e = std::make_shared<PlanEntry>();
+  e->key = key;
+  if (usp_status_t st = build_grid(e->g, B, S, H, D, causal, U, R, order, seq_lens, head_counts, o_dt))
+    return st;
+  const int oel = o_dt == USP_BF16 ? 2 : 4;
+  if (S > 0) {
+    usp_status_t st = e->g.fused_ring ? plan_fused(e->g, oel, e->plan) : plan_separate(e->g, oel, e->plan);
+    if (st) return st;
+  }
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  g_plan_cache.insert(g_plan_cache.begin(), e);
+  if (g_plan_cache.size() > kPlanCache) g_plan_cache.pop_back();
+  out = e;
+  return USP_OK;
+}
+
 void fill_relayout_grid(RelayoutParams& rp, const Grid& g, int d, int elem) {
   std::memset(&rp, 0, sizeof(rp));
   rp.B = g.B; rp.H = g.H; rp.D = d; rp.elem = elem; rp.R = g.R; rp.U = g.U;
   rp.seq_mode = 1; rp.S = g.S;
+  rp.seq_rs = int64_t(g.H) * d;
   int64_t row = 0;
   for (int r = 0; r < g.R; ++r) {
     rp.row0[r] = row;
@@ -299,10 +595,13 @@ void fill_relayout_grid(RelayoutParams& rp, const Grid& g, int d, int elem) {
     for (int u = 0; u < g.U; ++u) rp.hbase[r * g.U + u] = g.woff(r, u, d);
 }
 
-usp_status_t relayout_public(const void* src, void* dst, usp_dtype_t dt, int B, int H, int D, int P,
-                             const int32_t* seq_lens, const int32_t* head_counts, int dir,
-                             cudaStream_t stream) {
+usp_status_t relayout_public(int n_tensors, const void* const* src, void* const* dst, usp_dtype_t dt,
+                             int B, int H, int D, int P, const int32_t* seq_lens,
+                             const int32_t* head_counts, int dir, cudaStream_t stream) {
+  if (n_tensors < 1 || n_tensors > 3) return fail(USP_ERR_INVALID_ARG, "need 1 <= n_tensors <= 3");
   if (!src || !dst || !seq_lens) return fail(USP_ERR_INVALID_ARG, "NULL src, dst or seq_lens");
+  for (int t = 0; t < n_tensors; ++t)
+    if (!src[t] || !dst[t]) return fail(USP_ERR_INVALID_ARG, "NULL src[%d] or dst[%d]", t, t);
   if (dt != USP_BF16 && dt != USP_FP32) return fail(USP_ERR_INVALID_ARG, "dt must be BF16 or FP32");
   if (B < 1 || H < 1 || D < 1) return fail(USP_ERR_INVALID_ARG, "need B, H, D >= 1");
   if (P < 1 || P > kRelayoutMaxU) return fail(USP_ERR_INVALID_ARG, "need 1 <= P <= %d", kRelayoutMaxU);
@@ -334,11 +633,14 @@ usp_status_t relayout_public(const void* src, void* dst, usp_dtype_t dt, int B, 
   }
   if (S == 0) return USP_OK;
   if (usp_status_t st = check_device()) return st;
-  rp.src[0] = static_cast<const char*>(src);
-  rp.dst[0] = static_cast<char*>(dst);
-  rp.n_tensors = 1;
+  for (int t = 0; t < n_tensors; ++t) {
+    rp.src[t] = static_cast<const char*>(src[t]);
+    rp.dst[t] = static_cast<char*>(dst[t]);
+  }
+  rp.n_tensors = n_tensors;
   rp.B = B; rp.H = H; rp.D = D; rp.elem = elem; rp.R = 1; rp.U = P;
   rp.seq_mode = 0; rp.dir = dir; rp.S = static_cast<int>(S);
+  rp.seq_rs = int64_t(H) * D;
   rp.row0[0] = 0;
   rp.row0[1] = int64_t(B) * S;
   rp.S_r[0] = static_cast<int>(S);
@@ -359,14 +661,32 @@ extern "C" {
 usp_status_t usp_relayout_seq2head(const void* src, void* dst, usp_dtype_t dt, int B, int H, int D,
                                    int P, const int32_t* seq_lens, const int32_t* head_counts,
                                    usp_stream_t stream) {
-  return relayout_public(src, dst, dt, B, H, D, P, seq_lens, head_counts, 0,
+  void* d = dst;
+  return relayout_public(1, &src, &d, dt, B, H, D, P, seq_lens, head_counts, 0,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 usp_status_t usp_relayout_head2seq(const void* src, void* dst, usp_dtype_t dt, int B, int H, int D,
                                    int P, const int32_t* seq_lens, const int32_t* head_counts,
                                    usp_stream_t stream) {
-  return relayout_public(src, dst, dt, B, H, D, P, seq_lens, head_counts, 1,
+  void* d = dst;
+  return relayout_public(1, &src, &d, dt, B, H, D, P, seq_lens, head_counts, 1,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+usp_status_t usp_relayout_seq2head_multi(int n_tensors, const void* const* src, void* const* dst,
+                                         usp_dtype_t dt, int B, int H, int D, int P,
+                                         const int32_t* seq_lens, const int32_t* head_counts,
+                                         usp_stream_t stream) {
+  return relayout_public(n_tensors, src, dst, dt, B, H, D, P, seq_lens, head_counts, 0,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+usp_status_t usp_relayout_head2seq_multi(int n_tensors, const void* const* src, void* const* dst,
+                                         usp_dtype_t dt, int B, int H, int D, int P,
+                                         const int32_t* seq_lens, const int32_t* head_counts,
+                                         usp_stream_t stream) {
+  return relayout_public(n_tensors, src, dst, dt, B, H, D, P, seq_lens, head_counts, 1,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -460,19 +780,21 @@ usp_status_t usp_attn_partial(const void* q, const void* k, const void* v, int B
     kp.len[0] = Sk;
   }
   std::vector<AttnSeg> segs;
+  std::vector<AttnLink> links;
   for (const Run& r : plan_runs(qp, kp, q_pos != nullptr)) {
     AttnSeg s{};
     s.o = o; s.lse = lse;
-    s.q_map = 0; s.k_map = 1; s.v_map = 2;
+    s.q_map = 0;
     s.q_row0 = r.q0; s.q_len = r.q_len;
-    s.kv_row0 = 0; s.kv_len = r.kv_len;
-    s.diag = r.diag; s.n_heads = H;
+    s.link0 = static_cast<int>(links.size()); s.n_links = 1;
+    links.push_back({1, 2, 0, r.kv_len, r.diag});
+    s.n_heads = H;
     s.o_row0 = r.q0; s.o_bstride = Sq; s.o_heads = H;
     s.o_start0 = 0; s.o_len0 = INT_MAX; s.o_start1 = 0; s.o_stride = 1;
     s.rev = q_pos != nullptr;
     segs.push_back(s);
   }
-  return launch_attention(p, segs, D, reinterpret_cast<cudaStream_t>(stream));
+  return launch_attention(p, segs, links, D, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 usp_status_t usp_lse_merge(int n_parts, const float* o_parts, int64_t o_part_stride,
@@ -495,12 +817,12 @@ usp_status_t usp_lse_merge(int n_parts, const float* o_parts, int64_t o_part_str
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
-size_t usp_attention_workspace_size(int B, int S, int H, int D, int ulysses_degree,
+size_t usp_attention_workspace_size(int B, int S, int H, int D, int causal, int ulysses_degree,
                                     int ring_degree, usp_order_t order, usp_dtype_t o_dt) {
-  Grid g;
-  if (build_grid(g, B, S, H, D, ulysses_degree, ring_degree, order, nullptr, nullptr, o_dt) != USP_OK)
+  std::shared_ptr<const PlanEntry> pe;
+  if (get_plan(B, S, H, D, causal, ulysses_degree, ring_degree, order, nullptr, nullptr, o_dt, pe) != USP_OK)
     return 0;
-  return g.total;
+  return pe->g.total;
 }
 
 static usp_status_t attention_impl(const void* q, const void* k, const void* v, int B, int S, int H,
@@ -508,9 +830,10 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
                                    int ring_degree, const int32_t* seq_lens,
                                    const int32_t* head_counts, usp_order_t order, void* o,
                                    usp_dtype_t o_dt, float* lse, void* workspace,
-                                   size_t workspace_bytes, void* const* events, int* n_launches,
-                                   cudaStream_t stream) {
-  int launches = 0;
+                                   size_t workspace_bytes, void* const* events, int* launches,
+                                   int64_t in_rs, cudaStream_t stream) {
+  // in_rs: elements from one token's row of q (k, v) to the next: H*D, or 3*H*D for packed QKV
+  int n_launch[4] = {0, 0, 0, 0};
   auto mark = [&](int i) -> usp_status_t {
     if (events && events[i]) {
       cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream);
@@ -518,14 +841,15 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     }
     return USP_OK;
   };
-  if (n_launches) *n_launches = 0;
+  if (launches) for (int i = 0; i < 4; ++i) launches[i] = 0;
   if (!q || !k || !v || !o) return fail(USP_ERR_INVALID_ARG, "NULL q, k, v or o");
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)))
     return fail(USP_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
-  Grid g;
-  if (usp_status_t st = build_grid(g, B, S, H, D, ulysses_degree, ring_degree, order, seq_lens,
-                                   head_counts, o_dt))
+  std::shared_ptr<const PlanEntry> pe;
+  if (usp_status_t st = get_plan(B, S, H, D, causal, ulysses_degree, ring_degree, order, seq_lens,
+                                 head_counts, o_dt, pe))
     return st;
+  const Grid& g = pe->g;
   if (!workspace || !aligned(workspace, 256)) return fail(USP_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
   if (workspace_bytes < g.total)
     return fail(USP_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, g.total);
@@ -534,7 +858,6 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
   if (usp_status_t st = mark(0)) return st;
   char* ws = static_cast<char*>(workspace);
   const int U = g.U, R = g.R;
-  const int oel = o_dt == USP_BF16 ? 2 : 4;
   usp_status_t st;
 
   // 1. Q, K, V of virtual rank (r, u): in place in the global tensor when ring chunk r is one affine
@@ -544,20 +867,22 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     RelayoutParams rp;
     fill_relayout_grid(rp, g, D, 2);
     rp.n_tensors = 3;
+    rp.seq_rs = in_rs;
     rp.src[0] = static_cast<const char*>(q); rp.dst[0] = ws + g.off_q;
     rp.src[1] = static_cast<const char*>(k); rp.dst[1] = ws + g.off_k;
     rp.src[2] = static_cast<const char*>(v); rp.dst[2] = ws + g.off_v;
     rp.dir = 0;
     if ((st = launch_relayout(rp, stream))) return st;
-    ++launches;
+    ++n_launch[0];
   }
   if ((st = mark(1))) return st;
 
-  // 2. partial attention over every (Ulysses rank, q ring chunk, ring step) pair in one launch
+  // 2. attention over every (Ulysses rank, q ring chunk, ring step) pair in one launch: one
+  //    segment per chunk pair (ring partials or, with one ring rank, the final output), or one
+  //    chain per piece of query rows across all ring steps (fused ring: the final output)
   static thread_local AttnParams params;
   AttnParams& p = params;
   std::memset(&p, 0, sizeof(p));
-  auto map_index = [&](int r, int u, int t) { return (r * U + u) * 3 + t; };
   for (int r = 0; r < R; ++r) {
     for (int u = 0; u < U; ++u) {
       const void* base[3];
@@ -565,16 +890,16 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
       int64_t piece_rows = std::max(1, g.S_r[r]), piece_stride = 0;
       int n_pieces = 1;
       if (g.fused_in) {
-        const int64_t e0 = (int64_t(g.pos[r].start[0]) * H + g.hoff[u]) * D;
+        const int64_t e0 = int64_t(g.pos[r].start[0]) * in_rs + int64_t(g.hoff[u]) * D;
         base[0] = static_cast<const uint16_t*>(q) + e0;
         base[1] = static_cast<const uint16_t*>(k) + e0;
         base[2] = static_cast<const uint16_t*>(v) + e0;
-        row_stride = int64_t(g.pos[r].stride) * H * D;
-        batch_stride = int64_t(S) * H * D;
+        row_stride = int64_t(g.pos[r].stride) * in_rs;
+        batch_stride = int64_t(S) * in_rs;
         if (two_pieces(g.pos[r])) {  // zigzag chunk: its two half-chunks
           piece_rows = g.pos[r].len[0];
           n_pieces = 2;
-          piece_stride = int64_t(g.pos[r].start[1] - g.pos[r].start[0]) * H * D;
+          piece_stride = int64_t(g.pos[r].start[1] - g.pos[r].start[0]) * in_rs;
         }
       } else {
         const int64_t off = g.woff(r, u, D) * 2;
@@ -586,10 +911,11 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
       }
       if (B == 1) batch_stride = std::max<int64_t>(1, g.S_r[r]) * row_stride;
       for (int t = 0; t < 3; ++t) {
-        if ((st = make_qkv_map(&p.maps[map_index(r, u, t)], base[t], g.h[u], D, piece_rows, n_pieces, B,
-                               row_stride, piece_stride, batch_stride)))
+        const int mi = map_index(g, r, u, t);
+        if ((st = make_qkv_map(&p.maps[mi], base[t], g.h[u], D, piece_rows, n_pieces, B, row_stride,
+                               piece_stride, batch_stride)))
           return st;
-        p.map_rows[map_index(r, u, t)] = n_pieces > 1 ? static_cast<int>(piece_rows) : 0;
+        p.map_rows[mi] = n_pieces > 1 ? static_cast<int>(piece_rows) : 0;
       }
     }
   }
@@ -598,56 +924,28 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.budget_ns = wait_budget_ns();
   p.withhold_loads = withhold_loads();
-  // ring partials (fp32, head-sharded W layout) when R > 1; else the final output in place
-  const int64_t slot_o = g.elems * 4, slot_l = int64_t(B) * S * H;
-  p.o_bf16 = R > 1 ? 0 : (o_dt == USP_BF16);
-  std::vector<AttnSeg> segs;
-  for (int r = 0; r < R; ++r) {
-    for (int kstep = 0; kstep < R; ++kstep) {
-      const int r2 = (r - kstep + R) % R;
-      const std::vector<Run> runs = plan_runs(g.pos[r], g.pos[r2], causal != 0);
-      // a zigzag chunk addressed in place is two maps' worth of pieces: every run must start on a
-      // 128-row tile so that no tile straddles its half-chunks (runs start at 0 or at the second
-      // half for these orderings)
-      if (g.fused_in && two_pieces(g.pos[r]))
-        for (const Run& run : runs)
-          if (run.q0 % kAttnBM != 0)
-            return fail(USP_ERR_UNSUPPORTED, "zigzag run at row %d does not start on a 128-row tile", run.q0);
-      for (int u = 0; u < U; ++u) {
-        for (const Run& run : runs) {
-          AttnSeg s{};
-          s.q_map = map_index(r, u, 0);
-          s.k_map = map_index(r2, u, 1);
-          s.v_map = map_index(r2, u, 2);
-          s.q_row0 = run.q0; s.q_len = run.q_len;
-          s.kv_row0 = 0; s.kv_len = run.kv_len;
-          s.diag = run.diag; s.n_heads = g.h[u];
-          s.o_row0 = run.q0;
-          s.rev = causal != 0;
-          if (R > 1) {
-            s.o = ws + g.off_opart + kstep * slot_o + g.woff(r, u, D) * 4;
-            s.lse = reinterpret_cast<float*>(ws + g.off_lpart) + kstep * slot_l + g.woff(r, u, 1);
-            s.o_bstride = g.S_r[r]; s.o_heads = g.h[u];
-            s.o_start0 = 0; s.o_len0 = INT_MAX; s.o_start1 = 0; s.o_stride = 1;
-          } else {
-            s.o = static_cast<char*>(o) + int64_t(g.hoff[u]) * D * oel;
-            s.lse = lse ? lse + g.hoff[u] : nullptr;
-            s.o_bstride = S; s.o_heads = H;
-            s.o_start0 = g.pos[r].start[0]; s.o_len0 = g.pos[r].n_seg > 1 ? g.pos[r].len[0] : INT_MAX;
-            s.o_start1 = g.pos[r].start[1]; s.o_stride = g.pos[r].stride;
-          }
-          segs.push_back(s);
-        }
-      }
+  const bool partials = R > 1 && !g.fused_ring;
+  p.o_bf16 = partials ? 0 : (o_dt == USP_BF16);
+  // the cached plan's segments, bound to this call's output and workspace
+  std::vector<AttnSeg> segs = pe->plan.segs;
+  for (size_t i = 0; i < segs.size(); ++i) {
+    const SegOut& so = pe->plan.outs[i];
+    if (so.partial) {
+      segs[i].o = ws + so.o_off;
+      segs[i].lse = reinterpret_cast<float*>(ws + so.lse_off);
+    } else {
+      segs[i].o = static_cast<char*>(o) + so.o_off;
+      segs[i].lse = lse ? reinterpret_cast<float*>(reinterpret_cast<char*>(lse) + so.lse_off) : nullptr;
     }
   }
-  if ((st = launch_attention(p, segs, D, stream))) return st;
-  launches += static_cast<int>((segs.size() + kAttnMaxSegs - 1) / kAttnMaxSegs);
+  int n_att = 0;
+  if ((st = launch_attention(p, segs, pe->plan.links, D, stream, &n_att))) return st;
+  n_launch[1] = n_att;
   if ((st = mark(2))) return st;
 
   // 3. merge the ring partials straight into the global layout (the head -> seq all-to-all and the
   //    inverse reorder are the merge's store addressing)
-  if (R > 1) {
+  if (partials) {
     MergeMap mm;
     std::memset(&mm, 0, sizeof(mm));
     mm.n_blocks = R * U;
@@ -674,11 +972,11 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
                                reinterpret_cast<const float*>(ws + g.off_lpart), int64_t(B) * S * H,
                                int64_t(B) * S * H, D, o, o_dt == USP_BF16, lse, &mm, stream)))
       return st;
-    ++launches;
+    ++n_launch[2];
   }
   if ((st = mark(3))) return st;
   if ((st = mark(4))) return st;
-  if (n_launches) *n_launches = launches;
+  if (launches) for (int i = 0; i < 4; ++i) launches[i] = n_launch[i];
   return USP_OK;
 }
 
@@ -689,7 +987,22 @@ usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, i
                            size_t workspace_bytes, usp_stream_t stream) {
   return attention_impl(q, k, v, B, S, H, D, scale, causal, ulysses_degree, ring_degree, seq_lens,
                         head_counts, order, o, o_dt, lse, workspace, workspace_bytes, nullptr,
-                        nullptr, reinterpret_cast<cudaStream_t>(stream));
+                        nullptr, int64_t(H) * D, reinterpret_cast<cudaStream_t>(stream));
+}
+
+usp_status_t usp_attention_qkvpacked(const void* qkv, int B, int S, int H, int D, float scale,
+                                     int causal, int ulysses_degree, int ring_degree,
+                                     const int32_t* seq_lens, const int32_t* head_counts,
+                                     usp_order_t order, void* o, usp_dtype_t o_dt, float* lse,
+                                     void* workspace, size_t workspace_bytes,
+                                     usp_stream_t stream) {
+  if (!qkv) return fail(USP_ERR_INVALID_ARG, "NULL qkv");
+  const int64_t hd = int64_t(std::max(H, 0)) * std::max(D, 0);
+  const uint16_t* base = static_cast<const uint16_t*>(qkv);
+  return attention_impl(base, base + hd, base + 2 * hd, B, S, H, D, scale, causal, ulysses_degree,
+                        ring_degree, seq_lens, head_counts, order, o, o_dt, lse, workspace,
+                        workspace_bytes, nullptr, nullptr, 3 * hd,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 usp_status_t usp_attention_events(const void* q, const void* k, const void* v, int B, int S, int H,
@@ -697,11 +1010,19 @@ usp_status_t usp_attention_events(const void* q, const void* k, const void* v, i
                                   int ring_degree, const int32_t* seq_lens,
                                   const int32_t* head_counts, usp_order_t order, void* o,
                                   usp_dtype_t o_dt, float* lse, void* workspace,
-                                  size_t workspace_bytes, void* const* events, int* n_launches,
+                                  size_t workspace_bytes, void* const* events, int* launches,
                                   usp_stream_t stream) {
   return attention_impl(q, k, v, B, S, H, D, scale, causal, ulysses_degree, ring_degree, seq_lens,
                         head_counts, order, o, o_dt, lse, workspace, workspace_bytes, events,
-                        n_launches, reinterpret_cast<cudaStream_t>(stream));
+                        launches, int64_t(H) * D, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_attention_ring_mode(int B, int S, int H, int D, int causal, int ulysses_degree,
+                            int ring_degree, usp_order_t order, usp_dtype_t o_dt) {
+  std::shared_ptr<const PlanEntry> pe;
+  if (get_plan(B, S, H, D, causal, ulysses_degree, ring_degree, order, nullptr, nullptr, o_dt, pe) != USP_OK)
+    return -1;
+  return pe->g.R == 1 ? 0 : (pe->g.fused_ring ? 2 : 1);
 }
 
 usp_status_t usp_check_status(void* status, usp_stream_t stream) {
@@ -721,10 +1042,11 @@ usp_status_t usp_check_status(void* status, usp_stream_t stream) {
 
 int usp_plan_pairs(int S, int ulysses_degree, int ring_degree, int causal, usp_order_t order,
                    int32_t* out, int cap) {
-  Grid g;
-  if (build_grid(g, 1, S, std::max(1, ulysses_degree), 64, ulysses_degree, ring_degree, order,
-                 nullptr, nullptr, USP_FP32) != USP_OK)
+  std::shared_ptr<const PlanEntry> pe;
+  if (get_plan(1, S, std::max(1, ulysses_degree), 64, causal, ulysses_degree, ring_degree, order,
+               nullptr, nullptr, USP_FP32, pe) != USP_OK)
     return -1;
+  const Grid& g = pe->g;
   int n = 0;
   for (int u = 0; u < g.U; ++u) {
     for (int r = 0; r < g.R; ++r) {

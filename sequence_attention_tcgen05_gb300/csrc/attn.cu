@@ -88,19 +88,27 @@ struct Layout {
 struct Unit {
   const AttnSeg* seg;
   int b, h, q0, n_kv;
-  int qv[2];  // valid rows of tiles a and b
+  int last_row;  // last valid segment-local query row of the unit
+  int qv[2];     // valid rows of tiles a and b
 };
 
 __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
-  int lo = 0, hi = p.n_segs - 1;
+  int gl = 0, gh = p.n_groups - 1;
+  while (gl < gh) {
+    const int mid = (gl + gh + 1) >> 1;
+    if (p.groups[mid].unit0 <= unit) gl = mid; else gh = mid - 1;
+  }
+  const AttnGroup& G = p.groups[gl];
+  const int local = unit - G.unit0;
+  const int hb = local / G.blocks;
+  const int rem = local - hb * G.blocks;  // block index within the group's segments
+  int lo = G.seg0, hi = G.seg0 + G.n_segs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.segs[mid].unit0 <= unit) lo = mid; else hi = mid - 1;
+    if (p.segs[mid].qb0 <= rem) lo = mid; else hi = mid - 1;
   }
   const AttnSeg& s = p.segs[lo];
-  const int local = unit - s.unit0;
-  const int qi = local % s.n_qblk;
-  const int hb = local / s.n_qblk;
+  const int qi = rem - s.qb0;
   Unit u;
   u.seg = &s;
   const int qb = s.rev ? s.n_qblk - 1 - qi : qi;
@@ -109,11 +117,20 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
   u.q0 = qb * kAttnUnitRows;
   u.qv[0] = max(0, min(kAttnBM, s.q_len - u.q0));
   u.qv[1] = max(0, min(kAttnBM, s.q_len - u.q0 - kAttnBM));
-  const int last_row = u.q0 + u.qv[0] + u.qv[1] - 1;
-  int max_c = s.kv_len - 1;
-  if (s.diag != kNoDiag) max_c = min(max_c, last_row + s.diag);
-  u.n_kv = max_c < 0 ? 0 : max_c / kAttnBN + 1;
+  u.last_row = u.q0 + u.qv[0] + u.qv[1] - 1;
+  int n = 0;
+  for (int i = 0; i < s.n_links; ++i) n += link_tiles(p.links[s.link0 + i], u.last_row);
+  u.n_kv = n;
   return u;
+}
+
+// Units are dealt to the CTAs in a snake order: in round t CTA c takes unit t*G + c for even t and
+// t*G + G-1-c for odd t.  The host lists units longest first, so each CTA's total stays close to
+// the mean (a longest-processing-time deal) while neighbouring CTAs still work on the same head's
+// K/V at the same time, which keeps those tiles in L2.  Every role walks the same sequence.
+__device__ __forceinline__ int unit_of_round(int t) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return t * G + ((t & 1) ? G - 1 - c : c);
 }
 
 // Max over one row's 32 values of a 16x256b.x16 load (registers 4k + 2i + {0,1}, k < 16), then
@@ -134,17 +151,18 @@ __device__ __forceinline__ float row_max4(const uint32_t (&r)[64], int i) {
 // P = 2^(s * c + nb_i) for the thread's 64 values (row i uses nb_i), as bf16 pairs: the pair of
 // columns 8k + 2(t%4) + {0,1} (registers 4k + 2i + {0,1}, adjacent, so each packed fp32x2 op
 // reads a register pair as it is) is P column 4k + t%4, which is where a 16x128b store puts
-// register 2k + i.  Two stores of 32 P columns; returns the fp32 row sums of the unrounded values.
+// register 2k + i.  Four stores of 16 P columns (8 words each, so few P words are live at once);
+// returns the fp32 row sums of the unrounded values.
 __device__ __forceinline__ void exp_tile(const uint32_t (&r)[64], uint64_t c2, float nb0, float nb1,
                                          uint32_t t_p, float (&sum)[2]) {
   const uint64_t nbr[2] = {f2_pack(nb0, nb0), f2_pack(nb1, nb1)};
   uint64_t acc[2] = {0ull, 0ull};  // row 0, row 1
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t pk[16];
+  for (int quarter = 0; quarter < 4; ++quarter) {
+    uint32_t pk[8];
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int k = half * 8 + kk;
+    for (int kk = 0; kk < 4; ++kk) {
+      const int k = quarter * 4 + kk;
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const uint64_t a2 = f2_fma(f2_pack(__uint_as_float(r[4 * k + 2 * i]), __uint_as_float(r[4 * k + 2 * i + 1])),
@@ -156,7 +174,7 @@ __device__ __forceinline__ void exp_tile(const uint32_t (&r)[64], uint64_t c2, f
         pk[2 * kk + i] = pack_bf16x2(p0, p1);
       }
     }
-    tmem_st_16x128b_x8(t_p + half * 32, pk);
+    tmem_st_16x128b_x4(t_p + quarter * 16, pk);
   }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -224,7 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0, q_iter = 0;
       uint32_t kfills[STAGES], vfills[STAGES];
       for (int s = 0; s < STAGES; ++s) kfills[s] = vfills[s] = 0;
-      for (int unit = p.withhold_loads ? p.n_units : blockIdx.x; unit < p.n_units; unit += gridDim.x) {
+      const int rounds = p.withhold_loads ? 0 : (p.n_units + gridDim.x - 1) / gridDim.x;
+      for (int t = 0; t < rounds; ++t) {
+        const int unit = unit_of_round(t);
+        if (unit >= p.n_units) continue;
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
         const AttnSeg& s = *u.seg;
@@ -243,34 +264,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
         }
         ++q_iter;
-        const int kvrow = s.kv_row0;
-        const int kn = p.map_rows[s.k_map];  // the K and V maps of a run have the same pieces
-        int kr = kn ? kvrow % kn : kvrow, kp = kn ? kvrow / kn : 0;  // row, piece of the next tile
         bool ok = true;
-        for (int j = 0; j < u.n_kv; ++j) {
-          // K(j) may overwrite K(j - STAGES) once its score MMAs are done, well before the P V
-          // MMAs release V(j - STAGES).
-          if (!mbar_wait(&k_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
-          mbar_arrive_expect_tx(&k_full[stage], L::kKBytes);
+        // the unit's key tiles: every link in order, each from its own K/V maps
+        for (int li = 0; li < s.n_links && ok; ++li) {
+          const AttnLink& lk = p.links[s.link0 + li];
+          const int nl = link_tiles(lk, u.last_row);
+          const int kn = p.map_rows[lk.k_map];  // the K and V maps of a link have the same pieces
+          int kr = kn ? lk.kv_row0 % kn : lk.kv_row0, kp = kn ? lk.kv_row0 / kn : 0;  // row, piece
+          for (int j = 0; j < nl; ++j) {
+            // K(j) may overwrite K(j - STAGES) once its score MMAs are done, well before the P V
+            // MMAs release V(j - STAGES).
+            if (!mbar_wait(&k_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
+            mbar_arrive_expect_tx(&k_full[stage], L::kKBytes);
 #pragma unroll
-          for (int blk = 0; blk < D / 64; ++blk) {
-            uint8_t* dk = sm + L::kK + stage * L::kKBytes + blk * kAttnBN * 128;
-            if (kn == 0) tma_load_4d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, u.b, &k_full[stage]);
-            else tma_load_5d(dk, &p.maps[s.k_map], blk * 64, u.h, kr, kp, u.b, &k_full[stage]);
-          }
-          ++kfills[stage];
-          if (!mbar_wait(&v_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
-          mbar_arrive_expect_tx(&v_full[stage], L::kVBytes);
+            for (int blk = 0; blk < D / 64; ++blk) {
+              uint8_t* dk = sm + L::kK + stage * L::kKBytes + blk * kAttnBN * 128;
+              if (kn == 0) tma_load_4d(dk, &p.maps[lk.k_map], blk * 64, u.h, kr, u.b, &k_full[stage]);
+              else tma_load_5d(dk, &p.maps[lk.k_map], blk * 64, u.h, kr, kp, u.b, &k_full[stage]);
+            }
+            ++kfills[stage];
+            if (!mbar_wait(&v_empty[stage], phase ^ 1, abort_flag, p.status, budget)) { ok = false; break; }
+            mbar_arrive_expect_tx(&v_full[stage], L::kVBytes);
 #pragma unroll
-          for (int blk = 0; blk < D / 64; ++blk) {
-            uint8_t* dv = sm + L::kV + stage * L::kVBytes + blk * kAttnBN * 128;
-            if (kn == 0) tma_load_4d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, u.b, &v_full[stage]);
-            else tma_load_5d(dv, &p.maps[s.v_map], blk * 64, u.h, kr, kp, u.b, &v_full[stage]);
+            for (int blk = 0; blk < D / 64; ++blk) {
+              uint8_t* dv = sm + L::kV + stage * L::kVBytes + blk * kAttnBN * 128;
+              if (kn == 0) tma_load_4d(dv, &p.maps[lk.v_map], blk * 64, u.h, kr, u.b, &v_full[stage]);
+              else tma_load_5d(dv, &p.maps[lk.v_map], blk * 64, u.h, kr, kp, u.b, &v_full[stage]);
+            }
+            ++vfills[stage];
+            kr += kAttnBN;
+            if (kn && kr >= kn) { kr -= kn; ++kp; }
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
           }
-          ++vfills[stage];
-          kr += kAttnBN;
-          if (kn && kr >= kn) { kr -= kn; ++kp; }
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
       }
@@ -326,7 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ++gp[x];
         return true;
       };
-      for (int unit = blockIdx.x; unit < p.n_units && ok; unit += gridDim.x) {
+      const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+      for (int t = 0; t < rounds && ok; ++t) {
+        const int unit = unit_of_round(t);
+        if (unit >= p.n_units) continue;
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
         // Q and K/V come from TMA (async proxy, like the MMAs): the barrier waits order them, no
@@ -390,13 +418,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const bool r = mbar_wait(bar, parity, abort_flag, p.status, budget);
       return __all_sync(0xffffffffu, r);
     };
-    for (int unit = blockIdx.x; unit < p.n_units && ok; unit += gridDim.x) {
+    const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+    for (int t = 0; t < rounds && ok; ++t) {
+      const int unit = unit_of_round(t);
+      if (unit >= p.n_units) continue;
       const Unit u = decode_unit(p, unit);
       const AttnSeg& s = *u.seg;
       const int q0 = u.q0 + x * kAttnBM;  // first local row of this query tile
-      bool row_valid[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) row_valid[i] = rw[i] < u.qv[x];
+      auto row_valid_at = [&](int i) { return rw[i] < min(kAttnBM, s.q_len - q0); };
       // output element of row i's column 0 and its LSE index (computed where used, so that they
       // are not live across the key-tile loop)
       auto out_at = [&](int i, long long& oe, long long& la) {
@@ -411,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (u.n_kv == 0) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          if (!row_valid[i]) continue;
+          if (!row_valid_at(i)) continue;
           long long o_elem_i, lse_at_i;
           out_at(i, o_elem_i, lse_at_i);
           for (int k = 0; k < D / 8; ++k) {
@@ -425,24 +454,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         continue;
       }
-      int lim[2];  // visible key c <= lim (local key index)
-#pragma unroll
-      for (int i = 0; i < 2; ++i) lim[i] = s.diag == kNoDiag ? INT_MAX : q0 + rw[i] + s.diag;
       float m_ref[2] = {-INFINITY, -INFINITY};  // running max of scale*log2e*s, raised lazily
       float l[2] = {0.f, 0.f};                  // row sums over this thread's columns
-      for (int j = 0; j < u.n_kv; ++j, ++g) {
-        if (!wait_all(&s_full[x], g & 1)) { ok = false; break; }
+      // One key tile of link li: scores from TMEM, the mask where `masked`, the online softmax
+      // update, P back to TMEM.  Called from two loops per link so that the unmasked tiles carry no
+      // mask test at all.
+      auto tile = [&](int li, int j, bool masked) -> bool {
+        if (!wait_all(&s_full[x], g & 1)) return false;
         tc_fence_after();
         uint32_t r[64];
         tmem_ld_16x256b_x16(t_s, r);
         tmem_wait_ld();
-        const int c0 = j * kAttnBN;  // local key index of column 0
-        const bool need_mask =
-            (c0 + kAttnBN > s.kv_len) || (s.diag != kNoDiag && c0 + kAttnBN - 1 > q0 + s.diag);
-        if (need_mask) {
+        if (masked) {
+          const int kv_len = p.links[li].kv_len, diag = p.links[li].diag;
+          const int c0 = j * kAttnBN;  // link-local key index of column 0
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            const int last = min(s.kv_len - 1, lim[i]) - c0 - cq;  // visible: 8k + e <= last
+            // visible link-local keys c <= min(kv_len - 1, q0 + rw[i] + diag): 8k + e <= last
+            const int lim = diag == kNoDiag ? kv_len - 1 : min(kv_len - 1, q0 + rw[i] + diag);
+            const int last = lim - c0 - cq;
 #pragma unroll
             for (int k = 0; k < 16; ++k)
 #pragma unroll
@@ -496,6 +526,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[x]);
+        ++g;
+        return true;
+      };
+      // one online softmax over the key tiles of every link of the segment, in link order; a
+      // link's length and diagonal are re-read from the parameters where needed, so that only
+      // the link index and the tile counters stay live across the tiles
+      for (int li = s.link0; li < s.link0 + s.n_links && ok; ++li) {
+        // the unit's last valid row, from values that are live anyway
+        const int last_row = min(s.q_len, q0 - x * kAttnBM + kAttnUnitRows) - 1;
+        // tiles [0, mf) need no mask: whole tiles of keys that every row of this query tile sees
+        int mf = min(link_tiles(p.links[li], last_row), p.links[li].kv_len / kAttnBN);
+        if (p.links[li].diag != kNoDiag) {
+          const int d1 = q0 + p.links[li].diag + 1;  // keys [0, d1) are visible to the tile's first row
+          mf = min(mf, d1 <= 0 ? 0 : d1 / kAttnBN);
+        }
+        int j = 0;
+        for (; j < mf; ++j)
+          if (!tile(li, j, false)) { ok = false; break; }
+        if (!ok) break;
+        const int nl = link_tiles(p.links[li], min(s.q_len, q0 - x * kAttnBM + kAttnUnitRows) - 1);
+        for (; j < nl; ++j)
+          if (!tile(li, j, true)) { ok = false; break; }
       }
       if (!ok) break;
       // epilogue: full row sums from the four threads of each row, then O / l and the lse
@@ -525,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          if (!row_valid[i]) continue;
+          if (!row_valid_at(i)) continue;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const float v0 = __uint_as_float(o[4 * k + 2 * i]) * inv_l[i];
@@ -539,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if ((lane & 3) == 0 && s.lse) {
 #pragma unroll
         for (int i = 0; i < 2; ++i)
-          if (row_valid[i]) s.lse[lse_at[i]] = lse[i];
+          if (row_valid_at(i)) s.lse[lse_at[i]] = lse[i];
       }
     }
   }
@@ -560,10 +612,7 @@ usp_status_t launch_one(const AttnParams& p, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return fail(USP_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = std::max(1, std::min(p.n_units, sms));
+  const int grid = std::max(1, std::min(p.n_units, sm_count()));
   kern<<<grid, kThreads, L::kAlloc, stream>>>(p);
   return check_launch("attention kernel");
 }
@@ -614,36 +663,62 @@ usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D
   return USP_OK;
 }
 
-usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs, int D,
-                              cudaStream_t stream) {
+usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs,
+                              const std::vector<AttnLink>& links, int D, cudaStream_t stream,
+                              int* n_launched) {
+  if (n_launched) *n_launched = 0;
   if (!(p.scale_log2 > 0.f)) return fail(USP_ERR_INVALID_ARG, "the softmax scale must be positive");
-  // Longest units first: sort segments by the keys a full query block visits.
-  auto cost = [](const AttnSeg& s) {
-    return s.diag == kNoDiag ? s.kv_len : std::min(s.kv_len, s.q_len + s.diag);
+  // Segments grouped by unit group, longest first within a group: sort by the key tiles their
+  // longest query block visits.
+  auto cost = [&](const AttnSeg& s) {
+    long long c = 0;
+    for (int i = 0; i < s.n_links; ++i) c += link_tiles(links[s.link0 + i], s.q_len - 1);
+    return c;
   };
-  std::stable_sort(segs.begin(), segs.end(),
-                   [&](const AttnSeg& a, const AttnSeg& b) { return cost(a) > cost(b); });
+  std::stable_sort(segs.begin(), segs.end(), [&](const AttnSeg& a, const AttnSeg& b) {
+    return a.grp != b.grp ? a.grp < b.grp : cost(a) > cost(b);
+  });
   size_t at = 0;
   while (at < segs.size()) {
-    const size_t n = std::min<size_t>(kAttnMaxSegs, segs.size() - at);
-    int units = 0, used = 0;
-    for (size_t i = 0; i < n; ++i) {
-      AttnSeg s = segs[at + i];
+    long long units = 0;
+    int used = 0, n_links = 0, n_groups = 0;
+    for (; at < segs.size() && used < kAttnMaxSegs; ++at) {
+      AttnSeg s = segs[at];
+      if (s.n_links > kAttnMaxLinks) return fail(USP_ERR_UNSUPPORTED, "too many links in one segment");
+      if (n_links + s.n_links > kAttnMaxLinks) break;
       s.n_qblk = (s.q_len + kAttnUnitRows - 1) / kAttnUnitRows;
-      s.unit0 = units;
-      const long long add = static_cast<long long>(s.n_qblk) * s.n_heads * p.B;
-      if (add == 0) continue;
-      if (units + add > INT_MAX / 2) return fail(USP_ERR_UNSUPPORTED, "too many attention work units");
-      units += static_cast<int>(add);
+      if (s.n_qblk == 0) continue;  // (a segment whose links see no key still writes o = 0, lse = -inf)
+      const bool new_group = n_groups == 0 || p.segs[used - 1].grp != s.grp;
+      if (new_group) {
+        if (n_groups == kAttnMaxGroups) break;
+        if (n_groups > 0) {  // close the previous group
+          AttnGroup& G = p.groups[n_groups - 1];
+          units += static_cast<long long>(G.blocks) * p.segs[G.seg0].n_heads * p.B;
+        }
+        p.groups[n_groups++] = {static_cast<int>(units), 0, used, 0};
+      }
+      AttnGroup& G = p.groups[n_groups - 1];
+      s.qb0 = G.blocks;
+      G.blocks += s.n_qblk;
+      ++G.n_segs;
+      for (int i = 0; i < s.n_links; ++i) p.links[n_links + i] = links[s.link0 + i];
+      s.link0 = n_links;
+      n_links += s.n_links;
       p.segs[used++] = s;
     }
+    if (n_groups > 0) {
+      AttnGroup& G = p.groups[n_groups - 1];
+      units += static_cast<long long>(G.blocks) * p.segs[G.seg0].n_heads * p.B;
+    }
+    if (units > INT_MAX / 2) return fail(USP_ERR_UNSUPPORTED, "too many attention work units");
     p.n_segs = used;
-    p.n_units = units;
+    p.n_groups = n_groups;
+    p.n_units = static_cast<int>(units);
     if (units > 0) {
       usp_status_t st = D == 64 ? launch_one<64, 4>(p, stream) : launch_one<128, 2>(p, stream);
       if (st != USP_OK) return st;
+      if (n_launched) ++*n_launched;
     }
-    at += n;
   }
   return USP_OK;
 }

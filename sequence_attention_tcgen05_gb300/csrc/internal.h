@@ -17,6 +17,7 @@ namespace usp {
 usp_status_t fail(usp_status_t s, const char* fmt, ...);
 usp_status_t check_launch(const char* what);
 usp_status_t check_device();  // current device must be sm_103
+int sm_count();               // SMs of the current device (cached per device; 152 on a GB300)
 
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
@@ -57,6 +58,7 @@ struct RelayoutParams {
   int seq_mode;  // 0 packed chunks, 1 global through positions
   int dir;       // 0 sequence side -> head side, 1 head side -> sequence side
   int S;         // global sequence length (mode 1)
+  long long seq_rs;  // elements from one sequence-side row to the next (H * D unless packed)
   long long row0[kRelayoutMaxR + 1];
   int S_r[kRelayoutMaxR];
   int h[kRelayoutMaxU];
@@ -67,6 +69,7 @@ struct RelayoutParams {
   long long c_base[kRelayoutMaxRU];
   int p_start0[kRelayoutMaxR], p_len0[kRelayoutMaxR], p_start1[kRelayoutMaxR],
       p_stride[kRelayoutMaxR];  // mode 1
+  int sb_off[kRelayoutMaxU + 1];  // set by launch_relayout: first 32-vector sub-block of group g in a row
 };
 
 usp_status_t launch_relayout(RelayoutParams& p, cudaStream_t stream);
@@ -101,13 +104,24 @@ constexpr int kAttnBM = 128;  // query rows per tile (one TMEM lane each)
 constexpr int kAttnBN = 128;  // key rows per tile
 constexpr int kAttnUnitRows = 2 * kAttnBM;  // query rows per work unit (two tiles per CTA)
 constexpr int kAttnMaxMaps = 48;
-constexpr int kAttnMaxSegs = 128;
+constexpr int kAttnMaxSegs = 96;
+constexpr int kAttnMaxLinks = 256;
 constexpr int kNoDiag = INT_MAX;
 
-// One run of query rows against one key range: key c (0 <= c < kv_len) is visible to local
-// query row i (0 <= i < q_len) iff c <= i + diag (diag == kNoDiag: no limit).
-// Q/K/V tiles come from 4-D tensor maps {D, heads, rows, batch}; rows of this run are map rows
-// q_row0 + i (and kv_row0 + c).  Output row of query i of batch b:
+// One key range of a unit's online softmax: keys c (0 <= c < kv_len) of the K/V maps, map rows
+// kv_row0 + c; key c is visible to segment-local query row i iff c <= i + diag (diag == kNoDiag:
+// no limit).  A segment of one link is one ring step's (Q chunk, K/V chunk) pair; a segment of
+// several links is a chain: its query rows carry one online softmax across the K/V chunks of
+// every ring step (the ring merge done in registers), and it writes the final O and LSE.
+struct AttnLink {
+  int k_map, v_map;
+  int kv_row0, kv_len;
+  int diag;
+};
+
+// One run of query rows against the links [link0, link0 + n_links).  Q tiles come from 4-D (or
+// 5-D, two-piece) tensor maps {D, heads, rows, batch}; rows of this run are map rows q_row0 + i.
+// Output row of query i of batch b:
 //   row = b * o_bstride + pos(o_row0 + i),  pos(l) = l < o_len0 ? o_start0 + l * o_stride
 //                                                               : o_start1 + (l - o_len0) * o_stride
 // and element (row * o_heads + h) * D of `o` (LSE: row * o_heads + h of `lse`); `o` and `lse` are
@@ -115,22 +129,35 @@ constexpr int kNoDiag = INT_MAX;
 struct AttnSeg {
   void* o;        // fp32 or bf16 per launch
   float* lse;     // may be null
-  int q_map, k_map, v_map;
+  int q_map;
   int q_row0, q_len;
-  int kv_row0, kv_len;
-  int diag;
-  int n_heads;    // heads of the maps (work units per batch = n_qblk * n_heads)
+  int link0, n_links;
+  int n_heads;    // heads of the maps (the same for every segment of a group)
   int o_row0, o_bstride, o_heads;
   int o_start0, o_len0, o_start1, o_stride;
-  int n_qblk;     // 256-row query blocks
-  int unit0;
+  int grp;        // unit group (one per Ulysses rank): its segments share n_heads
+  int n_qblk;     // 256-row query blocks (set at launch)
+  int qb0;        // first block of this segment within its group (set at launch)
   int rev;        // 1: visit query blocks last first (causal: longest first)
+};
+
+// Work units of one group are numbered head-major: for every (batch, head), the query blocks of
+// all the group's segments (segments longest first, blocks in their visiting order).  All CTAs
+// working at the same time then share one or two heads' K/V, which stays in L2.
+constexpr int kAttnMaxGroups = 16;
+struct AttnGroup {
+  int unit0;      // first unit
+  int blocks;     // query blocks per (batch, head): sum of the segments' n_qblk
+  int seg0, n_segs;
 };
 
 struct AttnParams {
   CUtensorMap maps[kAttnMaxMaps];
   int map_rows[kAttnMaxMaps];  // two-piece maps: rows per piece (row l = piece l / n, row l % n); 0: one piece
   AttnSeg segs[kAttnMaxSegs];
+  AttnLink links[kAttnMaxLinks];
+  AttnGroup groups[kAttnMaxGroups];
+  int n_groups;
   int n_segs;
   int n_units;
   int B;
@@ -158,9 +185,20 @@ usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D
                           int n_pieces, int B, int64_t row_stride, int64_t piece_stride,
                           int64_t batch_stride);
 
-// Launch over all segments (split into several launches if there are more than fit).
-usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs, int D,
-                              cudaStream_t stream);
+// Launch over all segments, each with its own links (split into several launches if there are
+// more than fit; `n_launched`, if not null, receives how many).  The links of segs[i] are
+// links[segs[i].link0 .. + n_links) of `links`.
+usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs,
+                              const std::vector<AttnLink>& links, int D, cudaStream_t stream,
+                              int* n_launched);
+
+// Key tiles of a link visited by a 256-row query block whose last segment-local row is
+// `last_row` (host and device).
+__host__ __device__ inline int link_tiles(const AttnLink& lk, int last_row) {
+  int max_c = lk.kv_len - 1;
+  if (lk.diag != kNoDiag) max_c = max_c < last_row + lk.diag ? max_c : last_row + lk.diag;
+  return max_c < 0 ? 0 : max_c / kAttnBN + 1;
+}
 
 }  // namespace usp
 

@@ -4,8 +4,9 @@
 //   m = max_k lse_k,  w_k = 2^((lse_k - m) log2 e),  out = sum w_k out_k / sum w_k,
 //   lse = m + ln(sum w_k),
 // which is exact in real arithmetic and equal to applying the pairwise form in ring order.
-// Partials with lse = -inf saw no key: they get weight 0, and their out is not read (except by
-// the rows variant without a causal mask, which loads every slot with its LSE and ignores it).
+// Partials with lse = -inf saw no key: they get weight 0 and their out is never used.  The
+// public merge loads each partial's out together with its LSE (one memory latency per batch);
+// the rows variant of the causal path loads an out only once its LSE shows a visible key.
 //
 // HBM-bound: each thread owns float4 slots of D-vectors (a warp reads 512 contiguous bytes of each
 // partial for D = 128; the LSE loads of a vector are warp-uniform broadcasts).  The partial count
@@ -21,8 +22,9 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// NP partials, U vectors' worth of float4 slots per thread per iteration: all LSE loads first,
-// then every needed partial load, so that 2 x NP independent 16-byte loads are in flight.
+// NP partials, U vectors' worth of float4 slots per thread per iteration: every LSE and partial
+// load of the iteration is issued before the first is used (a partial whose LSE turns out to be
+// -inf was loaded for nothing but is ignored), so U x NP independent 16-byte loads are in flight.
 template <int NP, bool OUT_BF16, int U>
 __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict__ o_parts,
                                                         long long o_stride,
@@ -54,7 +56,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int k = 0; k < NP; ++k)
-        if (l[u][k] != -INFINITY)
+        if (valid[u])
           o[u][k] = __ldcs(reinterpret_cast<const float4*>(o_parts + k * o_stride + vec[u] * D) + q[u]);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -206,10 +208,11 @@ template <int NP>
 void launch_np(bool out_bf16, const MergeMap* map, unsigned blocks, cudaStream_t stream,
                const float* o_parts, long long o_stride, const float* lse_parts,
                long long lse_stride, long long n_vec, int D, void* o_out, float* lse_out) {
-  constexpr int U = NP <= 4 ? 2 : 1;
+  constexpr int U = NP <= 2 ? 4 : (NP <= 4 ? 2 : 1);
   if (map) {
     long long rb = (map->row0[map->n_blocks] + 7) / 8;
-    if (rb > 152LL * 32) rb = 152LL * 32;
+    const long long cap = static_cast<long long>(sm_count()) * 32;
+    if (rb > cap) rb = cap;
     const unsigned nb = static_cast<unsigned>(std::max(1LL, rb));
     auto go = [&](auto kern) {
       kern<<<nb, 256, 0, stream>>>(o_parts, o_stride, lse_parts, lse_stride, D, o_out, lse_out, *map);
@@ -223,12 +226,23 @@ void launch_np(bool out_bf16, const MergeMap* map, unsigned blocks, cudaStream_t
     }
     return;
   }
-  if (out_bf16)
-    lse_merge_kernel<NP, true, U><<<blocks, 256, 0, stream>>>(o_parts, o_stride, lse_parts,
-                                                              lse_stride, n_vec, D, o_out, lse_out);
-  else
-    lse_merge_kernel<NP, false, U><<<blocks, 256, 0, stream>>>(o_parts, o_stride, lse_parts,
-                                                               lse_stride, n_vec, D, o_out, lse_out);
+  // persistent grid: the CTAs that fit on the GPU at once (each thread then takes an equal share of
+  // the float4 slots, U at a time), never more threads than slots need
+  auto go = [&](auto kern) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    const long long slots = n_vec * (D / 4);
+    const long long need = (slots + 256LL * U - 1) / (256LL * U);
+    const long long ctas = std::max(1LL, std::min<long long>(static_cast<long long>(per_sm) * sm_count(), need));
+    kern<<<static_cast<unsigned>(ctas), 256, 0, stream>>>(o_parts, o_stride, lse_parts, lse_stride,
+                                                          n_vec, D, o_out, lse_out);
+  };
+  (void)blocks;
+  if (out_bf16) go(lse_merge_kernel<NP, true, U>);
+  else go(lse_merge_kernel<NP, false, U>);
 }
 
 }  // namespace
@@ -240,7 +254,8 @@ usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_
   if (n_vec == 0) return USP_OK;
   const long long total = n_vec * (D / 4);
   long long blocks = (total + 255) / 256;
-  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  const long long cap = static_cast<long long>(sm_count()) * 16;
+  if (blocks > cap) blocks = cap;
   const unsigned nb = static_cast<unsigned>(blocks);
 #define USP_MERGE_CASE(N)                                                                        \
   case N:                                                                                        \

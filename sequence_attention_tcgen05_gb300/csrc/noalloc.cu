@@ -7,8 +7,11 @@
 //
 // The scratch is a file-scope __device__ array of kScratchBytes.  Every GPU on which the library's
 // device code is loaded holds it until the process exits.  In host code the array's name is only a
-// host-side stand-in, so its device address is looked up with cudaGetSymbolAddress once per
-// device (on that device's first call, with the device current) and cached.
+// host-side stand-in, so its device address is looked up with cudaGetSymbolAddress, with the
+// device current, on the first call on each device and cached.  The cache entry remembers the
+// CUDA context it was taken in: if the device's context changes (cudaDeviceReset and a new
+// context, where the module and its array are loaded again), the next call looks the address up
+// again instead of using a stale one.
 //
 // All calls share the one array and it keeps the previous call's contents.  Only the status word
 // at its start must begin at zero, and each call clears it.  Calls that overlap on the GPU (other
@@ -26,7 +29,26 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_usp_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+  void* ctx = nullptr;   // CUcontext the address was looked up in
+  void* addr = nullptr;  // device address of g_usp_scratch in that context
+};
+ScratchEntry g_scratch[kMaxDevices];
+
+// The driver's cuCtxGetCurrent, reached through the runtime's entry-point query so that the library
+// does not link the driver library itself.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  return fn;
+}
 
 usp_status_t scratch_for_current_device(void** out) {
   int dev = 0;
@@ -37,8 +59,14 @@ usp_status_t scratch_for_current_device(void** out) {
   }
   if (dev < 0 || dev >= kMaxDevices)
     return usp::fail(USP_ERR_UNSUPPORTED, "usp_attention_noalloc: device ordinal %d >= %d", dev, kMaxDevices);
+  // The current context (null before the runtime has created it); the lookup below creates it.
+  CtxGetCurrentFn get_ctx = ctx_get_current();
+  if (!get_ctx) return usp::fail(USP_ERR_CUDA, "usp_attention_noalloc: cuCtxGetCurrent is not available");
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchEntry& ent = g_scratch[dev];
+  if (!ent.addr || !ctx || ent.ctx != static_cast<void*>(ctx)) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_usp_scratch);
     if (e != cudaSuccess || !p) {
@@ -46,9 +74,12 @@ usp_status_t scratch_for_current_device(void** out) {
       return usp::fail(USP_ERR_CUDA, "usp_attention_noalloc: cudaGetSymbolAddress of the scratch array: %s",
                        cudaGetErrorString(e));
     }
-    g_scratch_addr[dev] = p;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx)
+      return usp::fail(USP_ERR_CUDA, "usp_attention_noalloc: no current CUDA context on device %d", dev);
+    ent.ctx = ctx;
+    ent.addr = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = ent.addr;
   return USP_OK;
 }
 
@@ -60,7 +91,7 @@ extern "C" usp_status_t usp_attention_noalloc(const void* q, const void* k, cons
                                               const int32_t* seq_lens, const int32_t* head_counts,
                                               usp_order_t order, void* o, usp_dtype_t o_dt,
                                               float* lse, uint32_t* status, usp_stream_t stream) {
-  const size_t need = usp_attention_workspace_size(B, S, H, D, ulysses_degree, ring_degree, order, o_dt);
+  const size_t need = usp_attention_workspace_size(B, S, H, D, causal, ulysses_degree, ring_degree, order, o_dt);
   if (need == 0) {
     // invalid arguments: let usp_attention's validation report the precise error (it returns
     // before any launch when an argument is invalid)

@@ -176,4 +176,13 @@ WORKLOADS = {
     "qwen_1328_u2r2": Workload("qwen_1328_u2r2", 1, 24, 128, 7145, 2, 2),
     "llm_64k_ring8_zigzag": Workload("llm_64k_ring8_zigzag", 1, 32, 128, 65536, 1, 8,
                                      causal=True, order="zigzag"),
+    # Ring Anything / Ulysses Anything at large, uneven sizes: a sequence that no ring or head
+    # count divides (zigzag half-chunks of 4111 and 4112 rows, not whole 128-row tiles), an uneven
+    # stripe ring, and 24 heads over 5 Ulysses ranks (5/5/5/5/4 heads, 922/922/922/921/921 rows).
+    "llm_64k257_ring8_zigzag": Workload("llm_64k257_ring8_zigzag", 1, 32, 128, 65793, 1, 8,
+                                        causal=True, order="zigzag"),
+    "llm_32k_ring4_stripe": Workload("llm_32k_ring4_stripe", 1, 32, 128, 32771, 1, 4,
+                                     causal=True, order="stripe"),
+    "flux_1024_uaa5": Workload("flux_1024_uaa5", 1, 24, 128, 4608, 5, 1, text_rows=512,
+                               text_scale=0.5),
 }

@@ -18,9 +18,11 @@ USP_BF16, USP_FP32 = 0, 1
 ORDERS = {"contiguous": 0, "zigzag": 1, "stripe": 2}
 
 EXPORTED = [
-    "usp_relayout_seq2head", "usp_relayout_head2seq", "usp_reorder", "usp_attn_partial",
-    "usp_lse_merge", "usp_attention", "usp_attention_events", "usp_attention_noalloc",
-    "usp_attention_workspace_size",
+    "usp_relayout_seq2head", "usp_relayout_head2seq", "usp_relayout_seq2head_multi",
+    "usp_relayout_head2seq_multi", "usp_reorder", "usp_attn_partial",
+    "usp_lse_merge", "usp_attention", "usp_attention_qkvpacked", "usp_attention_events",
+    "usp_attention_noalloc",
+    "usp_attention_workspace_size", "usp_attention_ring_mode",
     "usp_check_status",
     "usp_plan_pairs", "usp_status_string", "usp_last_error", "usp_version",
 ]
@@ -66,18 +68,25 @@ def lib() -> ctypes.CDLL:
     sig = {
         "usp_relayout_seq2head": [vp, vp, i32, i32, i32, i32, i32, i32p, i32p, vp],
         "usp_relayout_head2seq": [vp, vp, i32, i32, i32, i32, i32, i32p, i32p, vp],
+        "usp_relayout_seq2head_multi": [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i32, i32,
+                                        i32, i32, i32p, i32p, vp],
+        "usp_relayout_head2seq_multi": [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i32, i32,
+                                        i32, i32, i32p, i32p, vp],
         "usp_reorder": [vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp],
         "usp_attn_partial": [vp, vp, vp, i32, i32, i32, i32, i32, i64, i64, f32, posp, posp, vp,
                              i32, vp, vp, vp],
         "usp_lse_merge": [i32, vp, i64, vp, i64, i64, i32, i32, vp, i32, vp, vp],
         "usp_attention": [vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, i32p, i32p, i32, vp,
                           i32, vp, vp, sz, vp],
+        "usp_attention_qkvpacked": [vp, i32, i32, i32, i32, f32, i32, i32, i32, i32p, i32p, i32, vp,
+                                    i32, vp, vp, sz, vp],
         "usp_attention_events": [vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, i32p, i32p,
                                  i32, vp, i32, vp, vp, sz, ctypes.POINTER(vp),
                                  ctypes.POINTER(ctypes.c_int), vp],
         "usp_attention_noalloc": [vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, i32p, i32p,
                                   i32, vp, i32, vp, vp, vp],
-        "usp_attention_workspace_size": [i32, i32, i32, i32, i32, i32, i32, i32],
+        "usp_attention_workspace_size": [i32, i32, i32, i32, i32, i32, i32, i32, i32],
+        "usp_attention_ring_mode": [i32, i32, i32, i32, i32, i32, i32, i32, i32],
         "usp_check_status": [vp, vp],
         "usp_plan_pairs": [i32, i32, i32, i32, i32, i32p, i32],
         "usp_status_string": [i32],
@@ -151,6 +160,30 @@ def usp_relayout_head2seq(src, dst, B, H, D, seq_lens, head_counts=None, dt=None
            "usp_relayout_head2seq")
 
 
+def _ptr_array(xs):
+    return (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+
+
+def usp_relayout_seq2head_multi(srcs, dsts, B, H, D, seq_lens, head_counts=None, dt=None,
+                                stream=None):
+    """seq->head re-layout of up to 3 same-shaped tensors (e.g. Q, K, V) in one launch."""
+    dt = _dtype(srcs[0]) if dt is None else dt
+    _check(lib().usp_relayout_seq2head_multi(len(srcs), _ptr_array(srcs), _ptr_array(dsts), dt, B,
+                                             H, D, len(seq_lens), _i32(seq_lens),
+                                             _i32(head_counts), _stream(stream)),
+           "usp_relayout_seq2head_multi")
+
+
+def usp_relayout_head2seq_multi(srcs, dsts, B, H, D, seq_lens, head_counts=None, dt=None,
+                                stream=None):
+    """head->seq re-layout of up to 3 same-shaped tensors in one launch."""
+    dt = _dtype(srcs[0]) if dt is None else dt
+    _check(lib().usp_relayout_head2seq_multi(len(srcs), _ptr_array(srcs), _ptr_array(dsts), dt, B,
+                                             H, D, len(seq_lens), _i32(seq_lens),
+                                             _i32(head_counts), _stream(stream)),
+           "usp_relayout_head2seq_multi")
+
+
 def usp_reorder(src, dst, B, S, H, D, R, order="contiguous", inverse=False, dt=None, stream=None):
     dt = _dtype(src) if dt is None else dt
     _check(lib().usp_reorder(_ptr(src), _ptr(dst), dt, B, S, H, D, R, ORDERS[order],
@@ -177,9 +210,23 @@ def usp_lse_merge(n_parts, o_parts, o_part_stride, lse_parts, lse_part_stride, n
 
 
 def usp_attention_workspace_size(B, S, H, D, ulysses_degree, ring_degree, order="contiguous",
-                                 o_dt=USP_FP32) -> int:
-    return int(lib().usp_attention_workspace_size(B, S, H, D, ulysses_degree, ring_degree,
-                                                  ORDERS[order], o_dt))
+                                 o_dt=USP_FP32, causal=False) -> int:
+    return int(lib().usp_attention_workspace_size(B, S, H, D, int(causal), ulysses_degree,
+                                                  ring_degree, ORDERS[order], o_dt))
+
+
+RING_MODES = {0: "none", 1: "separate", 2: "fused"}
+
+
+def usp_attention_ring_mode(B, S, H, D, causal, ulysses_degree, ring_degree, order="contiguous",
+                            o_dt=USP_FP32) -> str:
+    """How usp_attention runs the ring steps: "none" (one ring rank), "separate" (per-step fp32
+    partials and a merge pass) or "fused" (one online softmax per query block across all steps)."""
+    m = int(lib().usp_attention_ring_mode(B, S, H, D, int(causal), ulysses_degree, ring_degree,
+                                          ORDERS[order], o_dt))
+    if m < 0:
+        raise UspError(USP_ERR_INVALID_ARG, "usp_attention_ring_mode", lib().usp_last_error().decode())
+    return RING_MODES[m]
 
 
 def usp_attention(q, k, v, B, S, H, D, scale, causal, ulysses_degree, ring_degree, o, lse,
@@ -192,20 +239,33 @@ def usp_attention(q, k, v, B, S, H, D, scale, causal, ulysses_degree, ring_degre
                                workspace_bytes, _stream(stream)), "usp_attention")
 
 
+def usp_attention_qkvpacked(qkv, B, S, H, D, scale, causal, ulysses_degree, ring_degree, o, lse,
+                            workspace, workspace_bytes, seq_lens=None, head_counts=None,
+                            order="contiguous", o_dt=None, stream=None):
+    """usp_attention on a packed bf16 input qkv [B][S][3][H][D]."""
+    o_dt = _dtype(o) if o_dt is None else o_dt
+    _check(lib().usp_attention_qkvpacked(_ptr(qkv), B, S, H, D, float(scale), int(causal),
+                                         ulysses_degree, ring_degree, _i32(seq_lens),
+                                         _i32(head_counts), ORDERS[order], _ptr(o), o_dt,
+                                         _ptr(lse), _ptr(workspace), workspace_bytes,
+                                         _stream(stream)), "usp_attention_qkvpacked")
+
+
 def usp_attention_events(q, k, v, B, S, H, D, scale, causal, ulysses_degree, ring_degree, o, lse,
                          workspace, workspace_bytes, events, seq_lens=None, head_counts=None,
-                         order="contiguous", o_dt=None, stream=None) -> int:
-    """usp_attention that records 5 caller events between its phases; returns the launch count.
+                         order="contiguous", o_dt=None, stream=None) -> list[int]:
+    """usp_attention that records 5 caller events between its phases; returns the kernels it
+    launched per phase: [Q/K/V re-layout, attention, merge, output re-layout].
     ``events``: 5 raw cudaEvent_t handles (ints) or None entries."""
     o_dt = _dtype(o) if o_dt is None else o_dt
     ev = (ctypes.c_void_p * 5)(*[e or None for e in events])
-    n = ctypes.c_int(0)
+    n = (ctypes.c_int * 4)()
     _check(lib().usp_attention_events(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, float(scale),
                                       int(causal), ulysses_degree, ring_degree, _i32(seq_lens),
                                       _i32(head_counts), ORDERS[order], _ptr(o), o_dt, _ptr(lse),
-                                      _ptr(workspace), workspace_bytes, ev, ctypes.byref(n),
+                                      _ptr(workspace), workspace_bytes, ev, n,
                                       _stream(stream)), "usp_attention_events")
-    return n.value
+    return list(n)
 
 
 def usp_attention_noalloc(q, k, v, B, S, H, D, scale, causal, ulysses_degree, ring_degree, o, lse,
@@ -252,7 +312,8 @@ def attention(q, k, v, causal=False, ulysses_degree=1, ring_degree=1, order="con
     scale = D ** -0.5 if scale is None else scale
     o = torch.empty((B, S, H, D), dtype=out_dtype, device=q.device)
     lse = torch.empty((B, S, H), dtype=torch.float32, device=q.device)
-    nbytes = usp_attention_workspace_size(B, S, H, D, ulysses_degree, ring_degree, order, o_dt)
+    nbytes = usp_attention_workspace_size(B, S, H, D, ulysses_degree, ring_degree, order, o_dt,
+                                          causal)
     if nbytes == 0:
         raise UspError(USP_ERR_INVALID_ARG, "usp_attention_workspace_size",
                        lib().usp_last_error().decode())

@@ -65,11 +65,12 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.usp_lse_merge(17, 256, 0, 256, 0, 1, 1, 4, 256, 1, 256, None) == usp.USP_ERR_INVALID_ARG
 
 
-def test_workspace_size(L):
+def test_workspace_size(L, monkeypatch):
     B, S, H, D = 1, 4608, 24, 128
     # contiguous Ulysses: Q/K/V are addressed in place and O is written in place -> status only
     assert usp.usp_attention_workspace_size(B, S, H, D, 2, 1) == 256
-    # ring of 3: R fp32 partials of O and LSE
+    # ring of 3 with separate ring steps: R fp32 partials of O and LSE
+    monkeypatch.setenv("USP_RING_MERGE", "separate")
     r = usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3)
     assert 3 * 1000 * 4 * 64 * 4 + 3 * 1000 * 4 * 4 <= r <= 3 * 1000 * 4 * 64 * 4 + 3 * 1000 * 4 * 4 + 1024
     # zigzag ring: additionally the head-sharded bf16 copies of Q, K, V
@@ -79,11 +80,32 @@ def test_workspace_size(L):
     # addressed in place: the same size as contiguous order, no copies
     zc = usp.usp_attention_workspace_size(1, 65536, 32, 128, 1, 8, "contiguous")
     zz = usp.usp_attention_workspace_size(1, 65536, 32, 128, 1, 8, "zigzag")
-    assert zz == zc
+    assert zz == zc > 8 * 65536 * 32 * 128 * 4
     # half-chunks of 4095.5 rows on average (65535 tokens) are not whole tiles: copies again
     assert usp.usp_attention_workspace_size(1, 65535, 32, 128, 1, 8, "zigzag") > zc
+    # fused ring steps write the final output directly: no partial slots
+    monkeypatch.setenv("USP_RING_MERGE", "fused")
+    assert usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3) == 256
+    assert usp.usp_attention_workspace_size(1, 65536, 32, 128, 1, 8, "zigzag", causal=True) == 256
+    assert usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3, "zigzag") == z - (r - 256)
     assert usp.usp_attention_workspace_size(1, 10, 4, 96, 1, 1) == 0
     assert usp.usp_attention_workspace_size(1, 10, 4, 64, 5, 4) == 0
+
+
+def test_ring_mode_choice(L, monkeypatch):
+    """The ring mode follows the override, and without one the library's time model picks the
+    fused ring for the long causal zigzag ring (no 6.7 GB partial round trip, 8192 long units) and
+    the separate steps for a tiny ring whose units would not fill the GPU."""
+    monkeypatch.delenv("USP_RING_MERGE", raising=False)
+    assert usp.usp_attention_ring_mode(1, 4608, 24, 128, False, 2, 1) == "none"
+    assert usp.usp_attention_ring_mode(1, 65536, 32, 128, True, 1, 8, "zigzag", usp.USP_BF16) == "fused"
+    assert usp.usp_attention_ring_mode(1, 1000, 4, 64, False, 1, 3) == "separate"
+    for mode in ("fused", "separate"):
+        monkeypatch.setenv("USP_RING_MERGE", mode)
+        assert usp.usp_attention_ring_mode(1, 1000, 4, 64, False, 1, 3) == mode
+        assert usp.usp_attention_ring_mode(1, 1000, 4, 64, False, 1, 1) == "none"
+    with pytest.raises(usp.UspError):
+        usp.usp_attention_ring_mode(1, 10, 4, 96, False, 1, 2)
 
 
 @pytest.mark.parametrize("S,U,R,causal,order", [

@@ -27,10 +27,16 @@ def test_attention_flops():
     assert w["tiny_ring3"].attention_flops() == 4 * 4 * 64 * 1000 ** 2
 
 
-def test_no_reorder_pass_in_any_workload_step():
-    # every workload's chunks are addressed in place (zigzag 64K: 16 equal half-chunks of 4096)
+def test_reorder_pass_only_for_uneven_zigzag_chunks():
+    # the pages' workloads are addressed in place (zigzag 64K: 16 equal half-chunks of 4096); only
+    # zigzag half-chunks that are not whole 128-row tiles (65793 tokens: 4111/4112 rows) take the
+    # reorder + seq->head copy of Q, K and V, each element read once and written once
     for w in synth.WORKLOADS.values():
-        assert bench.phase_bytes(w, 2)["qkv_relayout"] == 0
+        b = bench.phase_bytes(w, 2, "separate")["qkv_relayout"]
+        if w.name == "llm_64k257_ring8_zigzag":
+            assert b == 2 * 3 * 65793 * 32 * 128 * 2
+        else:
+            assert b == 0, w.name
 
 
 def test_qwen_merge_bytes():
@@ -39,7 +45,9 @@ def test_qwen_merge_bytes():
     v = 7145 * 24
     expect = 2 * v * (128 * 4 + 4) + v * 128 * 2 + v * 4
     assert expect == 221552160
-    assert bench.phase_bytes(synth.WORKLOADS["qwen_1328_u2r2"], 2)["merge"] == expect
+    assert bench.phase_bytes(synth.WORKLOADS["qwen_1328_u2r2"], 2, "separate")["merge"] == expect
+    # fused ring steps have no merge pass
+    assert bench.phase_bytes(synth.WORKLOADS["qwen_1328_u2r2"], 2, "fused")["merge"] == 0
 
 
 def test_causal_zigzag_merge_bytes():
@@ -53,9 +61,9 @@ def test_causal_zigzag_merge_bytes():
     assert expect == 7323254784
     w = synth.WORKLOADS["llm_64k_ring8_zigzag"]
     assert bench.visible_partial_vectors(w) == seen
-    assert bench.phase_bytes(w, 2)["merge"] == expect
+    assert bench.phase_bytes(w, 2, "separate")["merge"] == expect
 
 
 def test_single_ring_rank_has_no_merge():
     for name in ("flux_1024_u2", "flux_1008_uaa2", "flux_1008_uaa3", "tiny_uaa3"):
-        assert bench.phase_bytes(synth.WORKLOADS[name], 2)["merge"] == 0
+        assert bench.phase_bytes(synth.WORKLOADS[name], 2, "none")["merge"] == 0

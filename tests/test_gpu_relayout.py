@@ -82,3 +82,27 @@ def test_reorder_bit_exact(order, B, S, H, D, R):
     torch().cuda.synchronize()
     back.check()
     assert np.array_equal(bits_of(back.view), src.reshape(-1))
+
+
+@pytest.mark.parametrize("B,H,D,lens,heads", [CASES[1], CASES[2], CASES[4]])
+def test_multi_tensor_relayout_bit_exact(B, H, D, lens, heads):
+    """Q, K, V in one launch (usp_relayout_seq2head_multi) and back (head2seq_multi): each tensor
+    bit-exact against the oracle's index loops, as if re-laid on its own."""
+    rng = np.random.default_rng(5)
+    S = sum(lens)
+    n = B * S * H * D
+    srcs = [rng.integers(0, 2**16, size=n, dtype=np.uint64).astype(np.uint16) for _ in range(3)]
+    xs = [_dev(x) for x in srcs]
+    ys = [Guarded((n,), xs[0].dtype) for _ in range(3)]
+    usp.usp_relayout_seq2head_multi(xs, [y.view for y in ys], B, H, D, lens, heads)
+    torch().cuda.synchronize()
+    for src, y in zip(srcs, ys):
+        y.check()
+        assert np.array_equal(bits_of(y.view), oracle.seq2head(src, B, H, D, lens, heads))
+    backs = [Guarded((n,), xs[0].dtype) for _ in range(3)]
+    usp.usp_relayout_head2seq_multi([y.view for y in ys], [b.view for b in backs], B, H, D, lens,
+                                    heads)
+    torch().cuda.synchronize()
+    for src, b in zip(srcs, backs):
+        b.check()
+        assert np.array_equal(bits_of(b.view), src)

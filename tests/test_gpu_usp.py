@@ -44,40 +44,58 @@ def test_tiny_uaa3_config():
 GRID = []
 for (U, R) in [(1, 1), (2, 1), (3, 1), (1, 2), (1, 3), (2, 2), (2, 3), (1, 8), (4, 4)]:
     for order in ["contiguous", "zigzag", "stripe"]:
-        GRID.append((U, R, order))
+        for mode in (["fused", "separate"] if R > 1 else ["none"]):
+            GRID.append((U, R, order, mode))
 
 
-@pytest.mark.parametrize("U,R,order", GRID)
+def set_ring_mode(monkeypatch, mode):
+    """Pins how usp_attention runs the ring steps (the library otherwise picks by its time
+    model): "fused" = one online softmax per query block across all ring steps, "separate" =
+    per-step fp32 partials and a merge pass."""
+    if mode in ("fused", "separate"):
+        monkeypatch.setenv("USP_RING_MERGE", mode)
+
+
+@pytest.mark.parametrize("U,R,order,mode", GRID)
 @pytest.mark.parametrize("causal", [False, True])
-def test_grid_small(U, R, order, causal):
+def test_grid_small(U, R, order, mode, causal, monkeypatch):
+    set_ring_mode(monkeypatch, mode)
     B, S, H, D = (2, 523, 5, 64) if (U + R) % 2 else (1, 777, 4, 128)
     if H < U:
         H = U
     o, l, (qb, kb, vb) = run_usp(B, S, H, D, U, R, causal, order, seed=U * 10 + R)
     ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), 1 / math.sqrt(D), causal)
-    check_attention(o, l, ro, rl, f"grid U={U} R={R} {order} causal={causal}")
+    check_attention(o, l, ro, rl, f"grid U={U} R={R} {order} causal={causal} ring={mode}")
 
 
+@pytest.mark.parametrize("mode", ["fused", "separate"])
 @pytest.mark.parametrize("B,S,H,D,U,R,causal", [
     (1, 512, 4, 64, 1, 2, True),      # half-chunks of 128 rows: one tile each
     (2, 2048, 4, 128, 2, 4, True),    # half-chunks of 256 rows, Ulysses 2 x ring 4
     (1, 3072, 3, 128, 1, 3, True),    # half-chunks of 512 rows, ring 3
+    (1, 1536, 2, 128, 1, 2, True),    # half-chunks of 384 rows: a 256-row block spans both
     (2, 1024, 4, 64, 2, 2, False),    # non-causal zigzag
 ])
-def test_zigzag_in_place_half_chunks(B, S, H, D, U, R, causal):
+def test_zigzag_in_place_half_chunks(B, S, H, D, U, R, causal, mode, monkeypatch):
     """Zigzag ring chunks of two equal half-chunks of whole 128-row tiles are read in place by
     two-piece tensor maps (no workspace copy); checked element by element against the oracle."""
+    set_ring_mode(monkeypatch, mode)
     assert S % (2 * R) == 0 and (S // (2 * R)) % 128 == 0
     o, l, (qb, kb, vb) = run_usp(B, S, H, D, U, R, causal, "zigzag", seed=S + R)
     ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), 1 / math.sqrt(D), causal)
-    check_attention(o, l, ro, rl, f"zigzag in place S={S} U={U} R={R} causal={causal}")
-    ws = usp.usp_attention_workspace_size(B, S, H, D, U, R, "zigzag", usp.USP_FP32)
-    # status word + ring partials only: no Q/K/V copies
+    check_attention(o, l, ro, rl, f"zigzag in place S={S} U={U} R={R} causal={causal} ring={mode}")
+    ws = usp.usp_attention_workspace_size(B, S, H, D, U, R, "zigzag", usp.USP_FP32, causal)
+    # status word (+ ring partials when separate) only: no Q/K/V copies
     rows_h = B * S * H
-    assert ws < 256 + R * (rows_h * D * 4 + rows_h * 4) + 4096 * R + 2 ** 20
+    if mode == "fused":
+        assert ws == 256
+    else:
+        assert ws < 256 + R * (rows_h * D * 4 + rows_h * 4) + 4096 * R + 2 ** 20
 
 
-def test_uneven_seq_lens_and_bf16_out():
+@pytest.mark.parametrize("mode", ["fused", "separate"])
+def test_uneven_seq_lens_and_bf16_out(mode, monkeypatch):
+    set_ring_mode(monkeypatch, mode)
     S, U, R = 1001, 2, 2
     ring = oracle.default_split(S, R)
     lens = [1, ring[0] - 1, ring[1] - 300, 300]
@@ -87,10 +105,29 @@ def test_uneven_seq_lens_and_bf16_out():
     check_attention(o, l, ro, rl, "uneven + bf16")
 
 
+_INPUTS = {}
+
+
+def _workload_inputs(w: synth.Workload):
+    """The workload's seeded Q, K, V bits, generated once per test module (the 64K inputs take a
+    while to generate on the host)."""
+    key = (w.B, w.S, w.H, w.D, w.seed, w.text_rows, w.text_scale)
+    if key not in _INPUTS:
+        _INPUTS.clear()
+        _INPUTS[key] = synth.make_qkv_bits(w.B, w.S, w.H, w.D, w.seed, w.text_rows, w.text_scale)
+    return _INPUTS[key]
+
+
 def _check_heads(w: synth.Workload, heads, rows=None):
-    o, l, (qb, kb, vb) = run_usp(w.B, w.S, w.H, w.D, w.ulysses_degree, w.ring_degree, w.causal,
-                                 w.order, list(w.seq_lens) or None, seed=w.seed,
-                                 text_rows=w.text_rows, text_scale=w.text_scale)
+    t = torch()
+    qb, kb, vb = _workload_inputs(w)
+    q, k, v = to_dev_bf16(qb), to_dev_bf16(kb), to_dev_bf16(vb)
+    o, l = usp.attention(q, k, v, causal=w.causal, ulysses_degree=w.ulysses_degree,
+                         ring_degree=w.ring_degree, order=w.order,
+                         seq_lens=list(w.seq_lens) or None, out_dtype=t.float32)
+    t.cuda.synchronize()
+    o, l = o.cpu().numpy(), l.cpu().numpy()
+    del q, k, v
     scale = 1 / math.sqrt(w.D)
     for h in heads:
         k = widen(kb[0, :, h]); v = widen(vb[0, :, h])
@@ -101,16 +138,81 @@ def _check_heads(w: synth.Workload, heads, rows=None):
 
 @pytest.mark.parametrize("name,heads", [("flux_1024_u2", [0, 11, 12, 23]),
                                         ("flux_1008_uaa2", [0, 12, 23]),
-                                        ("flux_1008_uaa3", [0, 8, 16, 23]),
-                                        ("qwen_1328_u2r2", [0, 12, 23])])
+                                        ("flux_1008_uaa3", [0, 8, 16, 23])])
 def test_full_size_workloads(name, heads):
     _check_heads(synth.WORKLOADS[name], heads)
 
 
-def test_long_context_causal_zigzag_sampled():
+@pytest.mark.parametrize("mode", ["fused", "separate"])
+def test_full_size_qwen(mode, monkeypatch):
+    set_ring_mode(monkeypatch, mode)
+    _check_heads(synth.WORKLOADS["qwen_1328_u2r2"], [0, 12, 23])
+
+
+@pytest.mark.parametrize("mode", ["fused", "separate"])
+def test_long_context_causal_zigzag_sampled(mode, monkeypatch):
+    set_ring_mode(monkeypatch, mode)
     w = synth.WORKLOADS["llm_64k_ring8_zigzag"]
     rng = np.random.default_rng(0)
     rows = np.unique(np.concatenate([rng.integers(0, w.S, 512), np.arange(0, 130),
                                      np.arange(w.S - 130, w.S), 4096 * np.arange(1, 16) - 1,
                                      4096 * np.arange(1, 16)]))
     _check_heads(w, [0, 31], rows)
+
+
+def _sampled_rows(w, n=512, seed=0):
+    """Random rows plus the first and last rows and both sides of every ring chunk boundary."""
+    rng = np.random.default_rng(seed)
+    bounds = set()
+    for pos in oracle.ring_positions(w.order, w.S, w.ring_degree):
+        steps = np.flatnonzero(np.diff(pos) != np.diff(pos)[:1]) if len(pos) > 1 else []
+        for i in [0, len(pos) - 1, *steps, *(np.asarray(steps) + 1)]:
+            if 0 <= i < len(pos):
+                bounds.add(int(pos[i]))
+    return np.unique(np.concatenate([rng.integers(0, w.S, n), np.arange(0, 130),
+                                     np.arange(w.S - 130, w.S), np.array(sorted(bounds))]))
+
+
+@pytest.mark.parametrize("mode", ["fused", "separate"])
+@pytest.mark.parametrize("name", ["llm_64k257_ring8_zigzag", "llm_32k_ring4_stripe"])
+def test_anything_large_uneven_causal(name, mode, monkeypatch):
+    """Ring Anything at large, uneven causal sizes: 65793 tokens over a zigzag ring of 8 (half-
+    chunks of 4111/4112 rows: the fused reorder + seq->head copy path) and 32771 tokens over a
+    stripe ring of 4; sampled rows of two heads against the oracle."""
+    set_ring_mode(monkeypatch, mode)
+    w = synth.WORKLOADS[name]
+    _check_heads(w, [0, w.H - 1], _sampled_rows(w))
+
+
+def test_ulysses_anything_24_heads_over_5():
+    """24 heads over 5 Ulysses ranks (5/5/5/5/4) at FLUX 1024^2 length: every head of the last,
+    smaller group and the heads on both sides of each group boundary, all rows."""
+    w = synth.WORKLOADS["flux_1024_uaa5"]
+    _check_heads(w, [0, 4, 5, 9, 10, 14, 15, 19, 20, 21, 22, 23])
+
+
+@pytest.mark.parametrize("U,R,order,causal,mode", [
+    (1, 1, "contiguous", False, "none"), (2, 1, "contiguous", True, "none"),
+    (1, 3, "zigzag", True, "fused"), (1, 3, "zigzag", True, "separate"),   # zigzag copy path
+    (2, 2, "stripe", True, "fused"), (1, 2, "zigzag", True, "separate"),
+    (3, 2, "contiguous", False, "fused"),
+])
+def test_qkvpacked_matches_oracle(U, R, order, causal, mode, monkeypatch):
+    """usp_attention_qkvpacked on a [B][S][3][H][D] input: the tensor maps read the packed rows in
+    place (3*H*D row stride), and the zigzag copy path reads them directly."""
+    set_ring_mode(monkeypatch, mode)
+    t = torch()
+    B, S, H, D = (2, 1000, 4, 128) if order != "zigzag" or R != 2 else (1, 1024, 3, 128)
+    qb, kb, vb = synth.make_qkv_bits(B, S, H, D, seed=7)
+    packed = np.ascontiguousarray(np.stack([qb, kb, vb], axis=2))  # [B][S][3][H][D]
+    qkv = to_dev_bf16(packed)
+    o = t.empty((B, S, H, D), dtype=t.float32, device="cuda")
+    lse = t.empty((B, S, H), dtype=t.float32, device="cuda")
+    nbytes = usp.usp_attention_workspace_size(B, S, H, D, U, R, order, usp.USP_FP32, causal)
+    ws = t.zeros(nbytes, dtype=t.uint8, device="cuda")
+    usp.usp_attention_qkvpacked(qkv, B, S, H, D, 1 / math.sqrt(D), causal, U, R, o, lse, ws,
+                                nbytes, order=order)
+    assert usp.usp_check_status(ws) == usp.USP_OK
+    ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), 1 / math.sqrt(D), causal)
+    check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl,
+                    f"qkvpacked U={U} R={R} {order} causal={causal} ring={mode}")

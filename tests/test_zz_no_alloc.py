@@ -4,53 +4,64 @@ synchronisation).  It runs on a 128 MiB scratch array built into the library ins
 workspace.
 
 This file is named to be collected last, so that a run stopping at its first failure has run every
-other test before these.  The GPU test calls the entry point through the C ABI twice in a row, on
-two different problems, and checks each result against usp_attention with a torch-allocated
-workspace, within the tolerances the parity tests use; the second call also shows that the first
-call's leftovers in the shared scratch do not leak into the next result."""
+other test before these.  The GPU test calls the entry point through the C ABI three times in a
+row on different problems and checks each result element by element against the fp64 oracle at
+the parity tests' tolerances.  The first two calls run the ring steps separately, so their fp32
+partials live in the shared scratch: the second call is causal with another ordering and grid, and
+its fully masked chunk pairs leave partial slots that it must not read, so anything it picked up
+from the first call's leftovers would show in its result.  The third call runs the fused ring."""
 import math
 
 import numpy as np
 import pytest
 
+import oracle
 from sequence_attention_tcgen05_gb300 import build, synth, usp
 
+O_MAX_ABS, O_MEAN_ABS, LSE_MAX_ABS = 2e-2, 2e-3, 1e-3
 
-def _run_pair(t, B, S, H, D, U, R, causal, order, out_dtype, seed):
+
+def _call_and_check(t, B, S, H, D, U, R, causal, order, out_dtype, seed):
     qb, kb, vb = synth.make_qkv_bits(B, S, H, D, seed)
     q, k, v = (t.from_numpy(x.view(np.int16)).view(t.bfloat16).cuda() for x in (qb, kb, vb))
-    ref_o, ref_l = usp.attention(q, k, v, causal=causal, ulysses_degree=U, ring_degree=R,
-                                 order=order, out_dtype=out_dtype)
     o = t.full((B, S, H, D), float("nan"), dtype=out_dtype, device="cuda")
     lse = t.full((B, S, H), float("nan"), dtype=t.float32, device="cuda")
     status = t.full((1,), 7, dtype=t.int32, device="cuda")
     usp.usp_attention_noalloc(q, k, v, B, S, H, D, 1.0 / math.sqrt(D), causal, U, R, o, lse,
                               order=order, status=status)
     assert usp.usp_check_status(status) == usp.USP_OK
-    t.cuda.synchronize()
-    d_o = (o.float() - ref_o.float()).abs()
-    fin = t.isfinite(ref_l)
-    assert bool((t.isfinite(lse) == fin).all())
-    assert float(d_o.max()) <= 2e-2 and float(d_o.mean()) <= 2e-3
-    assert float((lse[fin] - ref_l[fin]).abs().max()) <= 1e-3
-    return float(d_o.max())
+    ref_o, ref_l = oracle.attention(oracle.widen_bf16(qb), oracle.widen_bf16(kb),
+                                    oracle.widen_bf16(vb), 1.0 / math.sqrt(D), causal)
+    got_o = o.float().cpu().numpy().astype(np.float64)
+    got_l = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got_o))
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(got_l), fin)
+    err = np.abs(got_o - ref_o)
+    assert err.max() <= O_MAX_ABS and err.mean() <= O_MEAN_ABS, (err.max(), err.mean())
+    assert np.abs(got_l[fin] - ref_l[fin]).max() <= LSE_MAX_ABS
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_point_twice():
+def test_noalloc_matches_oracle_three_calls(monkeypatch):
     import torch as t
     build.build_library()
-    # ring of 3, causal, zigzag, fp32 out; then Ulysses 2 x ring 2, non-causal, bf16 out
-    e1 = _run_pair(t, 1, 1000, 4, 64, 1, 3, True, "zigzag", t.float32, seed=1)
-    e2 = _run_pair(t, 1, 777, 6, 128, 2, 2, False, "contiguous", t.bfloat16, seed=2)
-    assert e1 == 0.0 and e2 == 0.0  # same kernels on the same inputs: identical results
+    monkeypatch.setenv("USP_RING_MERGE", "separate")
+    # ring of 3, contiguous, non-causal, fp32 out: every partial slot written
+    _call_and_check(t, 1, 1000, 4, 64, 1, 3, False, "contiguous", t.float32, seed=1)
+    # Ulysses 2 x ring 2, stripe, causal, bf16 out, other shapes: masked pairs leave slots unread
+    _call_and_check(t, 1, 777, 6, 128, 2, 2, True, "stripe", t.bfloat16, seed=2)
+    monkeypatch.setenv("USP_RING_MERGE", "fused")
+    # ring of 4, zigzag, causal, fp32 out, fused ring steps
+    _call_and_check(t, 2, 600, 3, 128, 1, 4, True, "zigzag", t.float32, seed=3)
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
-    """FLUX-sized ring-2 fp32 output needs far more than 128 MiB: rejected before any launch."""
+    """A 64K-token zigzag ring of 8 whose half-chunks are not whole 128-row tiles (65535 tokens)
+    needs head-sharded copies of Q, K and V (1.6 GB): rejected before any launch."""
     build.build_library()
     L = usp.lib()
-    st = L.usp_attention_noalloc(256, 256, 256, 1, 65536, 32, 128, 0.08, 1, 1, 8, None, None, 1,
+    st = L.usp_attention_noalloc(256, 256, 256, 1, 65535, 32, 128, 0.08, 1, 1, 8, None, None, 1,
                                  256, usp.USP_FP32, 256, None, None)
     assert st == usp.USP_ERR_WORKSPACE
     msg = L.usp_last_error().decode()
