@@ -69,7 +69,6 @@ struct RelayoutParams {
   long long c_base[kRelayoutMaxRU];
   int p_start0[kRelayoutMaxR], p_len0[kRelayoutMaxR], p_start1[kRelayoutMaxR],
       p_stride[kRelayoutMaxR];  // mode 1
-  int sb_off[kRelayoutMaxU + 1];  // set by launch_relayout: first 32-vector sub-block of group g in a row
 };
 
 usp_status_t launch_relayout(RelayoutParams& p, cudaStream_t stream);

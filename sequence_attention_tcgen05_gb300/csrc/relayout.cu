@@ -3,13 +3,12 @@
 // and their fusion.  Pure data movement, bit-exact, HBM-bound.
 //
 // Every (tensor, row, head group) moves one contiguous block of h_g * D elements on both sides
-// (h_g * D * elem bytes: 3 KB for 12 bf16 heads of 128).  The blocks are cut into sub-blocks of
-// 32 vectors (512 bytes with 16-byte vectors; the widest vector every offset allows), numbered
-// tensor-major, then row, head group and position in the block.  The grid is persistent (as many
-// CTAs as fit on the GPU at once) and every warp takes an equal, contiguous range of sub-blocks,
-// so all warps finish together whatever the block count.  A warp issues the loads of up to kNV
-// sub-blocks of one row (one vector per lane each) before their stores, so it keeps 4 KB in
-// flight and places each row once.
+// (h_g * D * elem bytes: 3 KB for 12 bf16 heads of 128).  One warp copies one block: its lanes
+// issue every 16-byte (or narrower, when an offset is not aligned) vector load of the block, up
+// to kNV per lane, before the first store, so a warp keeps the whole block in flight and waits
+// for one memory latency per block.  Blocks are numbered tensor-major, then row, then head
+// group, so the warps of a CTA read neighbouring memory on the sequence side; with one block per
+// warp the hardware's CTA scheduler balances the work.
 #include <algorithm>
 #include <cstdio>
 
@@ -67,52 +66,44 @@ __device__ __forceinline__ RowPlace place_row(const RelayoutParams& p, long long
   return x;
 }
 
-constexpr int kNV = 8;  // sub-blocks (one vector per lane each) in flight per warp
+constexpr int kNV = 8;  // vectors in flight per lane (4 KB per warp with 16-byte vectors)
 
+// One warp per (tensor, row, head group) block: the lanes issue every vector load of the block
+// (up to kNV per lane per batch) before the first store.
 template <int VEC>
-__global__ void __launch_bounds__(256) relayout_kernel(const __grid_constant__ RelayoutParams p,
-                                                       long long n_sb) {
+__global__ void __launch_bounds__(256) relayout_block_kernel(const __grid_constant__ RelayoutParams p,
+                                                             long long n_blocks) {
   using T = typename Vec<VEC>::T;
   const int lane = threadIdx.x & 31;
-  const long long W = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  const long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  long long s = n_sb * w / W;  // this warp's sub-blocks [s, e)
-  const long long e = n_sb * (w + 1) / W;
-  const int sbpr = p.sb_off[p.U];  // sub-blocks per row (all groups)
   const long long rows = p.row0[p.R];
-  while (s < e) {
-    const long long q = s / sbpr;  // tensor * rows + row
-    int j = static_cast<int>(s - q * sbpr);
-    const int tensor = static_cast<int>(q / rows);
-    const long long row = q - tensor * rows;
-    const int nb = static_cast<int>(min(static_cast<long long>(min(kNV, sbpr - j)), e - s));
+  const long long per_tensor = rows * p.U;
+  const long long step = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long blk = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       blk < n_blocks; blk += step) {
+    const int tensor = static_cast<int>(blk / per_tensor);
+    const long long rest = blk - tensor * per_tensor;
+    const long long row = rest / p.U;
+    const int g = static_cast<int>(rest - row * p.U);
     const RowPlace x = place_row(p, row);
-    const long long row_in_r = static_cast<long long>(x.b) * p.S_r[x.r] + x.l;
-    int g = 0;
-    while (p.sb_off[g + 1] <= j) ++g;
-    T buf[kNV];
-    T* dp[kNV];
+    const long long hg = static_cast<long long>(p.h[g]) * p.D;
+    const long long head_elem = p.hbase[x.r * p.U + g] + (static_cast<long long>(x.b) * p.S_r[x.r] + x.l) * hg;
+    const long long seq_g = x.seq_elem + static_cast<long long>(p.hoff[g]) * p.D;
+    const int nvec = static_cast<int>(hg * p.elem / VEC);
+    const T* __restrict__ src = reinterpret_cast<const T*>(p.src[tensor] + (p.dir == 0 ? seq_g : head_elem) * p.elem);
+    T* __restrict__ dst = reinterpret_cast<T*>(p.dst[tensor] + (p.dir == 0 ? head_elem : seq_g) * p.elem);
+    for (int v0 = 0; v0 < nvec; v0 += 32 * kNV) {
+      T buf[kNV];
 #pragma unroll
-    for (int i = 0; i < kNV; ++i) {
-      dp[i] = nullptr;
-      if (i < nb) {
-        while (p.sb_off[g + 1] <= j) ++g;
-        const long long hg = static_cast<long long>(p.h[g]) * p.D;
-        const long long head_elem = p.hbase[x.r * p.U + g] + row_in_r * hg;
-        const long long seq_g = x.seq_elem + static_cast<long long>(p.hoff[g]) * p.D;
-        const int v = (j - p.sb_off[g]) * 32 + lane;
-        if (v < static_cast<int>(hg * p.elem / VEC)) {
-          const T* src = reinterpret_cast<const T*>(p.src[tensor] + (p.dir == 0 ? seq_g : head_elem) * p.elem);
-          buf[i] = __ldcs(src + v);
-          dp[i] = reinterpret_cast<T*>(p.dst[tensor] + (p.dir == 0 ? head_elem : seq_g) * p.elem) + v;
-        }
-        ++j;
+      for (int i = 0; i < kNV; ++i) {
+        const int v = v0 + i * 32 + lane;
+        if (v < nvec) buf[i] = __ldcs(src + v);
+      }
+#pragma unroll
+      for (int i = 0; i < kNV; ++i) {
+        const int v = v0 + i * 32 + lane;
+        if (v < nvec) dst[v] = buf[i];
       }
     }
-#pragma unroll
-    for (int i = 0; i < kNV; ++i)
-      if (dp[i]) *dp[i] = buf[i];
-    s += nb;
   }
 }
 
@@ -189,27 +180,17 @@ usp_status_t launch_relayout(RelayoutParams& p, cudaStream_t stream) {
     }
     return check_launch("relayout kernel");
   }
-  // sub-blocks of 32 vectors per (row, group): prefix over the groups of a row
-  p.sb_off[0] = 0;
-  for (int u = 0; u < p.U; ++u)
-    p.sb_off[u + 1] = p.sb_off[u] + static_cast<int>((static_cast<long long>(p.h[u]) * p.D * p.elem / g + 31) / 32);
-  const long long n_sb = total * p.sb_off[p.U] * p.n_tensors;
-  // persistent grid: the CTAs that fit on the GPU at once, never more warps than sub-blocks
-  const int threads = 256;
-  auto go = [&](auto kern) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess || per_sm < 1) {
-      cudaGetLastError();
-      per_sm = 1;
-    }
-    long long ctas = std::min<long long>(static_cast<long long>(per_sm) * sms, (n_sb + 7) / 8);
-    kern<<<static_cast<unsigned>(std::max(1LL, ctas)), threads, 0, stream>>>(p, n_sb);
-  };
+  // one warp per (tensor, row, head group) block, 8 warps per CTA; the hardware hands CTAs to the
+  // SMs as slots free up (a grid-stride loop takes over beyond 2^24 CTAs)
+  const long long n_blocks = total * p.U * p.n_tensors;
+  long long ctas = (n_blocks + 7) / 8;
+  if (ctas > (1LL << 24)) ctas = 1LL << 24;
+  const unsigned grid = static_cast<unsigned>(ctas);
   switch (g) {
-    case 16: go(relayout_kernel<16>); break;
-    case 8: go(relayout_kernel<8>); break;
-    case 4: go(relayout_kernel<4>); break;
-    default: go(relayout_kernel<2>); break;
+    case 16: relayout_block_kernel<16><<<grid, 256, 0, stream>>>(p, n_blocks); break;
+    case 8: relayout_block_kernel<8><<<grid, 256, 0, stream>>>(p, n_blocks); break;
+    case 4: relayout_block_kernel<4><<<grid, 256, 0, stream>>>(p, n_blocks); break;
+    default: relayout_block_kernel<2><<<grid, 256, 0, stream>>>(p, n_blocks); break;
   }
   return check_launch("relayout kernel");
 }
