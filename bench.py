@@ -56,14 +56,16 @@ NOMINAL_HBM_GBS = 8000.0
 # dram__bytes_write.sum from one ncu capture of that workload's launch, with the hash of the kernel
 # sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
-    "flux_1024_u2": {"bytes": 89264896, "kernel_hash": "15fcae45c593c630"},
+    # one full-size launch: dram__bytes_read.sum 3.70 GB + dram__bytes_write.sum 573.50 MB (ncu
+    # prints three significant digits for the read figure)
+    "llm_64k_ring8_zigzag": {"bytes": 3700000000 + 573500000, "kernel_hash": "899953450e061c0c"},
 }
 L2_BYTES = 129e6
 
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("attn.cu", "ptx.cuh", "internal.h"):
+    for f in ("attn.cu", "ptx.cuh"):
         with open(os.path.join(ROOT, "sequence_attention_tcgen05_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -330,6 +332,23 @@ def standalone_relayout(w, q, k, v, o, flush, stream, reps: int = 30):
                              "buffer_sets": n_in, "launches": 1},
             "head2seq_o": {"GB/s": bout / (us_out * 1e-6) / 1e9, "bytes": bout, "us": us_out,
                            "buffer_sets": n_out, "launches": 1}}
+
+
+def torch_copy_GBs(nbytes: int, flush, stream, reps: int = 30) -> float:
+    """GB/s (bytes read + written) of torch's device-to-device copy of a tensor of nbytes / 2
+    bytes, timed like the standalone legs: the practical ceiling for a transfer of that size."""
+    import torch
+    n = max(1, nbytes // 4)  # bf16 elements of half the traffic
+    sets = [(torch.empty(n, dtype=torch.bfloat16, device="cuda"),
+             torch.empty(n, dtype=torch.bfloat16, device="cuda")) for _ in range(rotation(nbytes))]
+
+    def launch(i):
+        a, b = sets[i]
+        b.copy_(a)
+
+    us = back_to_back_us(launch, len(sets), reps, flush, stream)
+    del sets
+    return 2 * n * 2 / (us * 1e-6) / 1e9
 
 
 def standalone_merge(w, out_dt, flush, stream, reps: int = 30):
@@ -719,10 +738,24 @@ def run_ours(args):
     nvtx.range_push("bench: standalone re-layout and merge")
     standalone = standalone_relayout(w, q, k, v, o, flush, stream)
     standalone_m = standalone_merge(w, out_dt, flush, stream)
+    # the same legs on the FLUX 1024^2 shape (57 MB tensors) when the workload is another one
+    flux_legs = None
+    if w.name != "flux_1024_u2":
+        wf = workload("flux_1024_u2")
+        shape = (wf.B, wf.S, wf.H, wf.D)
+        qf, kf, vf = (torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(3))
+        of = torch.zeros(shape, dtype=out_dt, device=device)
+        flux_legs = {"workload": wf.name, "relayout": standalone_relayout(wf, qf, kf, vf, of, flush, stream),
+                     "merge": standalone_merge(wf, out_dt, flush, stream)}
+        del qf, kf, vf, of
     nvtx.range_pop()
-    for part in (standalone["seq2head_qkv"], standalone["head2seq_o"], standalone_m):
+    legs = [standalone["seq2head_qkv"], standalone["head2seq_o"], standalone_m]
+    if flux_legs:
+        legs += [flux_legs["relayout"]["seq2head_qkv"], flux_legs["relayout"]["head2seq_o"], flux_legs["merge"]]
+    for part in legs:
         part["frac_measured_hbm"] = part["GB/s"] / peaks["hbm_gbs"]
         part["frac_8TBs"] = part["GB/s"] / NOMINAL_HBM_GBS
+        part["torch_copy_same_bytes_GB/s"] = torch_copy_GBs(part["bytes"], flush, stream)
     bw_s = sum(phases[n] for n in ("qkv_relayout", "merge") if ran[n]) / 1000.0 / breakdown_steps
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -741,7 +774,7 @@ def run_ours(args):
                            "frac_measured_hbm": (bw_bytes / bw_s / 1e9 / peaks["hbm_gbs"]) if bw_s > 0 else None,
                            "frac_8TBs": (bw_bytes / bw_s / 1e9 / NOMINAL_HBM_GBS) if bw_s > 0 else None,
                            "phases": bw, "standalone_relayout": standalone,
-                           "standalone_merge": standalone_m},
+                           "standalone_merge": standalone_m, "standalone_flux_1024_shape": flux_legs},
         "phases_ms_per_step": {k: (v / breakdown_steps if ran[k] else None)
                                for k, v in phases.items()},
         "phase_launches": dict(zip(phases, phase_launches)),

@@ -65,6 +65,48 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.usp_lse_merge(17, 256, 0, 256, 0, 1, 1, 4, 256, 1, 256, None) == usp.USP_ERR_INVALID_ARG
 
 
+def test_new_entry_points_validate_on_host(L):
+    """The packed-QKV and multi-tensor entry points reject bad arguments before any launch."""
+    lens = (ctypes.c_int32 * 2)(3, 4)
+    two = (ctypes.c_void_p * 2)(256, 512)
+    with_null = (ctypes.c_void_p * 2)(256, None)
+    for f in (L.usp_relayout_seq2head_multi, L.usp_relayout_head2seq_multi):
+        assert f(0, two, two, 0, 1, 4, 8, 2, lens, None, None) == usp.USP_ERR_INVALID_ARG
+        assert f(4, two, two, 0, 1, 4, 8, 2, lens, None, None) == usp.USP_ERR_INVALID_ARG
+        assert f(2, two, with_null, 0, 1, 4, 8, 2, lens, None, None) == usp.USP_ERR_INVALID_ARG
+        assert "dst[1]" in L.usp_last_error().decode()
+    # packed QKV: NULL input, misaligned input, D not built, workspace too small
+    assert L.usp_attention_qkvpacked(None, 1, 10, 4, 64, 1.0, 0, 1, 1, None, None, 0, 256, 1, 256,
+                                     256, 1 << 20, None) == usp.USP_ERR_INVALID_ARG
+    assert L.usp_attention_qkvpacked(258, 1, 10, 4, 64, 1.0, 0, 1, 1, None, None, 0, 256, 1, 256,
+                                     256, 1 << 20, None) == usp.USP_ERR_INVALID_ARG
+    assert L.usp_attention_qkvpacked(256, 1, 10, 4, 96, 1.0, 0, 1, 1, None, None, 0, 256, 1, 256,
+                                     256, 1 << 20, None) == usp.USP_ERR_UNSUPPORTED
+    assert L.usp_attention_qkvpacked(256, 1, 10, 4, 64, 1.0, 0, 1, 2, None, None, 0, 256, 1, 256,
+                                     256, 16, None) == usp.USP_ERR_WORKSPACE
+
+
+def test_plans_are_reused_and_follow_the_override(L, monkeypatch):
+    """Planning a long ring takes milliseconds; the library caches plans per argument set, so a
+    repeated query is fast, and the USP_RING_MERGE override is part of the key."""
+    import time
+    monkeypatch.delenv("USP_RING_MERGE", raising=False)
+    args = (1, 69632, 32, 128, 1, 1, 8, 1, 0)  # a shape no other test plans (16 half-chunks of 4352)
+    t0 = time.perf_counter()
+    first = L.usp_attention_ring_mode(*args)
+    t1 = time.perf_counter()
+    for _ in range(20):
+        assert L.usp_attention_ring_mode(*args) == first
+    t2 = time.perf_counter()
+    assert (t2 - t1) / 20 < max(1e-3, (t1 - t0) / 10)
+    monkeypatch.setenv("USP_RING_MERGE", "separate")
+    assert L.usp_attention_ring_mode(*args) == 1
+    assert L.usp_attention_workspace_size(*args) > 8 * 69632 * 32 * 128 * 4
+    monkeypatch.setenv("USP_RING_MERGE", "fused")
+    assert L.usp_attention_ring_mode(*args) == 2
+    assert L.usp_attention_workspace_size(*args) == 256
+
+
 def test_workspace_size(L, monkeypatch):
     B, S, H, D = 1, 4608, 24, 128
     # contiguous Ulysses: Q/K/V are addressed in place and O is written in place -> status only
