@@ -56,9 +56,8 @@ NOMINAL_HBM_GBS = 8000.0
 # dram__bytes_write.sum from one ncu capture of that workload's launch, with the hash of the kernel
 # sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
-    # one full-size launch: dram__bytes_read.sum 3.70 GB + dram__bytes_write.sum 573.50 MB (ncu
-    # prints three significant digits for the read figure)
-    "llm_64k_ring8_zigzag": {"bytes": 3700000000 + 573500000, "kernel_hash": "899953450e061c0c"},
+    # one full-size launch: dram__bytes_read.sum 3836886528 + dram__bytes_write.sum 574490624
+    "llm_64k_ring8_zigzag": {"bytes": 3836886528 + 574490624, "kernel_hash": "b1ed7830221165e0"},
 }
 L2_BYTES = 129e6
 

@@ -1,6 +1,14 @@
-// Partial attention on the 5th-generation tensor cores: for every (chunk pair, batch, head,
-// 256-row query block) work unit, O = softmax(scale Q K^T + mask) V and its natural-log LSE
-// ([USP] the backend's (out, lse) for one ring step; [CP] Ring Attention).
+// Attention on the 5th-generation tensor cores: for every (segment, batch, head, 256-row query
+// block) work unit, O = softmax(scale Q K^T + mask) V and its natural-log LSE ([USP] the backend's
+// (out, lse) for one ring step; [CP] Ring Attention).  A segment's keys are one or more links
+// (key ranges of K/V chunks): with one link a unit is one ring step's chunk pair and may write an
+// fp32 partial; with several, the unit's online softmax runs across the K/V chunks of every ring
+// step in ring order (the LSE-weighted merge done in registers) and writes the final O and LSE.
+//
+// Work units are numbered per unit group (one per Ulysses rank), head-major over the group's
+// segments (longest first), and dealt to the CTAs in a snake order: the longest units go first,
+// each CTA's total stays close to the mean, and CTAs running at the same time share one or two
+// heads' K/V in L2.
 //
 // One persistent CTA per SM, five warpgroups (640 threads):
 //   WG0  warp 0: TMA producer — the unit's two 128-row Q tiles, then K and V tiles into a
@@ -22,7 +30,10 @@
 //                + 8) and a quarter of their 128 key columns (8k + 2(t%4) + {0,1}), read with one
 //                16-lane tcgen05.ld (.16x256b.x16).  Row maxima and sums combine over the four
 //                threads of a row with two warp shuffles, so the two warpgroups of a tile never
-//                wait for each other.  Masking on boundary tiles, 2^(s * scale log2e - m) with packed
+//                wait for each other.  A tile that needs a mask (past a link's last key, or past
+//                the causal diagonal) first gets -inf written into its hidden S columns in TMEM by
+//                a small pre-pass; launches without such tiles use a kernel instantiation without
+//                that code.  2^(s * scale log2e - m) with packed
 //                fp32x2 fused multiply-adds and MUFU ex2; each thread's column pair becomes one
 //                bf16x2 P word that a .16x128b tcgen05.st puts exactly at P column 4k + t%4, so P
 //                for the tile's 128 keys is packed over S_x columns [0, 64).  Once a warp's rows
@@ -151,18 +162,20 @@ __device__ __forceinline__ float row_max4(const uint32_t (&r)[64], int i) {
 // P = 2^(s * c + nb_i) for the thread's 64 values (row i uses nb_i), as bf16 pairs: the pair of
 // columns 8k + 2(t%4) + {0,1} (registers 4k + 2i + {0,1}, adjacent, so each packed fp32x2 op
 // reads a register pair as it is) is P column 4k + t%4, which is where a 16x128b store puts
-// register 2k + i.  Four stores of 16 P columns (8 words each, so few P words are live at once);
-// returns the fp32 row sums of the unrounded values.
+// register 2k + i.  PARTS stores of 64 / PARTS P columns (PARTS = 4 keeps fewer P words live, for
+// the kernels whose registers are tightest); returns the fp32 row sums of the unrounded values.
+template <int PARTS>
 __device__ __forceinline__ void exp_tile(const uint32_t (&r)[64], uint64_t c2, float nb0, float nb1,
                                          uint32_t t_p, float (&sum)[2]) {
+  constexpr int KP = 16 / PARTS;
   const uint64_t nbr[2] = {f2_pack(nb0, nb0), f2_pack(nb1, nb1)};
   uint64_t acc[2] = {0ull, 0ull};  // row 0, row 1
 #pragma unroll
-  for (int quarter = 0; quarter < 4; ++quarter) {
-    uint32_t pk[8];
+  for (int quarter = 0; quarter < PARTS; ++quarter) {
+    uint32_t pk[2 * KP];
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const int k = quarter * 4 + kk;
+    for (int kk = 0; kk < KP; ++kk) {
+      const int k = quarter * KP + kk;
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const uint64_t a2 = f2_fma(f2_pack(__uint_as_float(r[4 * k + 2 * i]), __uint_as_float(r[4 * k + 2 * i + 1])),
@@ -174,7 +187,8 @@ __device__ __forceinline__ void exp_tile(const uint32_t (&r)[64], uint64_t c2, f
         pk[2 * kk + i] = pack_bf16x2(p0, p1);
       }
     }
-    tmem_st_16x128b_x4(t_p + quarter * 16, pk);
+    if constexpr (PARTS == 4) tmem_st_16x128b_x4(t_p + quarter * 16, pk);
+    else tmem_st_16x128b_x8(t_p + quarter * 32, pk);
   }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -184,7 +198,9 @@ __device__ __forceinline__ void exp_tile(const uint32_t (&r)[64], uint64_t c2, f
   }
 }
 
-template <int D, int STAGES>
+// MASKS = false: the launch has no tile that needs a mask (every link whole key tiles, no causal
+// diagonal), so the kernel carries only the unmasked tile loop.
+template <int D, int STAGES, bool MASKS>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using L = Layout<D, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -456,30 +472,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       float m_ref[2] = {-INFINITY, -INFINITY};  // running max of scale*log2e*s, raised lazily
       float l[2] = {0.f, 0.f};                  // row sums over this thread's columns
-      // One key tile of link li: scores from TMEM, the mask where `masked`, the online softmax
-      // update, P back to TMEM.  Called from two loops per link so that the unmasked tiles carry no
-      // mask test at all.
-      auto tile = [&](int li, int j, bool masked) -> bool {
+      // One key tile: scores from TMEM, the online softmax update, P back to TMEM.  The
+      // mask-free kernel (MASKS = false) runs `tile` on every tile; the other runs `tile_masked`,
+      // which first writes -inf into the hidden columns of a tile that needs a mask (a small
+      // TMEM pre-pass, so the tile body itself carries no mask code).  The two bodies are kept
+      // apart because each instantiation's register allocation is at its limit.
+      auto tile = [&]() -> bool {
         if (!wait_all(&s_full[x], g & 1)) return false;
         tc_fence_after();
         uint32_t r[64];
         tmem_ld_16x256b_x16(t_s, r);
         tmem_wait_ld();
-        if (masked) {
-          const int kv_len = p.links[li].kv_len, diag = p.links[li].diag;
-          const int c0 = j * kAttnBN;  // link-local key index of column 0
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            // visible link-local keys c <= min(kv_len - 1, q0 + rw[i] + diag): 8k + e <= last
-            const int lim = diag == kNoDiag ? kv_len - 1 : min(kv_len - 1, q0 + rw[i] + diag);
-            const int last = lim - c0 - cq;
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-#pragma unroll
-              for (int e = 0; e < 2; ++e)
-                if (8 * k + e > last) r[4 * k + 2 * i + e] = 0xff800000u;  // -inf
-          }
-        }
         float alpha[2] = {1.f, 1.f};
         bool resc = false;
         float sum[2];
@@ -488,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // for the P stores, then redo the tile after raising m.
         bool fast = __all_sync(0xffffffffu, m_ref[0] != -INFINITY && m_ref[1] != -INFINITY);
         if (fast) {
-          exp_tile(r, c2, -m_ref[0], -m_ref[1], t_s, sum);
+          exp_tile<2>(r, c2, -m_ref[0], -m_ref[1], t_s, sum);
           fast = __all_sync(0xffffffffu, sum[0] <= kFastSum && sum[1] <= kFastSum);
           if (!fast) tmem_wait_st();
         }
@@ -506,7 +509,81 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
           const float nb0 = m_ref[0] == -INFINITY ? 0.f : -m_ref[0];
           const float nb1 = m_ref[1] == -INFINITY ? 0.f : -m_ref[1];
-          exp_tile(r, c2, nb0, nb1, t_s, sum);
+          exp_tile<2>(r, c2, nb0, nb1, t_s, sum);
+        }
+        l[0] = l[0] * alpha[0] + sum[0];
+        l[1] = l[1] * alpha[1] + sum[1];
+        if (__any_sync(0xffffffffu, resc)) {
+          // S_x(j) complete => P V of tile j-1 complete: O_x is stable
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t w[32];
+            tmem_ld_16x256b_x8(t_o + cc * 64, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha[(i >> 1) & 1]);
+            tmem_st_16x256b_x8(t_o + cc * 64, w);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[x]);
+        ++g;
+        return true;
+      };
+      auto tile_masked = [&](int li, int j, bool masked) -> bool {
+        if (!wait_all(&s_full[x], g & 1)) return false;
+        tc_fence_after();
+        if (masked) {
+          const int kv_len = p.links[li].kv_len, diag = p.links[li].diag;
+          const int c0 = j * kAttnBN;  // link-local key index of column 0
+          uint32_t m[64];
+          tmem_ld_16x256b_x16(t_s, m);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int lim = diag == kNoDiag ? kv_len - 1 : min(kv_len - 1, q0 + rw[i] + diag);
+            const int last = lim - c0 - cq;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+#pragma unroll
+              for (int e = 0; e < 2; ++e)
+                if (8 * k + e > last) m[4 * k + 2 * i + e] = 0xff800000u;  // -inf
+          }
+          tmem_st_16x256b_x16(t_s, m);
+          tmem_wait_st();
+        }
+        uint32_t r[64];
+        tmem_ld_16x256b_x16(t_s, r);
+        tmem_wait_ld();
+        float alpha[2] = {1.f, 1.f};
+        bool resc = false;
+        float sum[2];
+        // Fast path: exponentials against the running max as it stands.  A partial sum above
+        // kFastSum (or inf / NaN) means some score rose more than 11 log2 units above m: wait
+        // for the P stores, then redo the tile after raising m.
+        bool fast = __all_sync(0xffffffffu, m_ref[0] != -INFINITY && m_ref[1] != -INFINITY);
+        if (fast) {
+          exp_tile<D == 64 ? 4 : 2>(r, c2, -m_ref[0], -m_ref[1], t_s, sum);
+          fast = __all_sync(0xffffffffu, sum[0] <= kFastSum && sum[1] <= kFastSum);
+          if (!fast) tmem_wait_st();
+        }
+        if (!fast) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float mx = row_max4(r, i) * c;
+            if (mx > m_ref[i] + kTau) {
+              if (m_ref[i] != -INFINITY) {
+                alpha[i] = ex2_approx(m_ref[i] - mx);
+                resc = true;
+              }
+              m_ref[i] = mx;
+            }
+          }
+          const float nb0 = m_ref[0] == -INFINITY ? 0.f : -m_ref[0];
+          const float nb1 = m_ref[1] == -INFINITY ? 0.f : -m_ref[1];
+          exp_tile<D == 64 ? 4 : 2>(r, c2, nb0, nb1, t_s, sum);
         }
         l[0] = l[0] * alpha[0] + sum[0];
         l[1] = l[1] * alpha[1] + sum[1];
@@ -542,12 +619,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           mf = min(mf, d1 <= 0 ? 0 : d1 / kAttnBN);
         }
         int j = 0;
-        for (; j < mf; ++j)
-          if (!tile(li, j, false)) { ok = false; break; }
-        if (!ok) break;
-        const int nl = link_tiles(p.links[li], min(s.q_len, q0 - x * kAttnBM + kAttnUnitRows) - 1);
-        for (; j < nl; ++j)
-          if (!tile(li, j, true)) { ok = false; break; }
+        if constexpr (!MASKS) {
+          for (; j < mf; ++j)
+            if (!tile()) { ok = false; break; }
+          if (!ok) break;
+        } else {
+          // tiles j >= mf get their hidden columns set to -inf in TMEM first
+          const int nl = link_tiles(p.links[li], last_row);
+          for (; j < nl; ++j)
+            if (!tile_masked(li, j, j >= mf)) { ok = false; break; }
+        }
       }
       if (!ok) break;
       // epilogue: full row sums from the four threads of each row, then O / l and the lse
@@ -605,11 +686,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   }
 }
 
-template <int D, int STAGES>
+template <int D, int STAGES, bool MASKS>
 usp_status_t launch_one(const AttnParams& p, cudaStream_t stream) {
   using L = Layout<D, STAGES>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  auto kern = attn_fwd_kernel<D, STAGES>;
+  auto kern = attn_fwd_kernel<D, STAGES, MASKS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return fail(USP_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   const int grid = std::max(1, std::min(p.n_units, sm_count()));
@@ -715,7 +796,12 @@ usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs,
     p.n_groups = n_groups;
     p.n_units = static_cast<int>(units);
     if (units > 0) {
-      usp_status_t st = D == 64 ? launch_one<64, 4>(p, stream) : launch_one<128, 2>(p, stream);
+      // the mask-free kernel when every link is whole key tiles without a causal diagonal
+      bool masks = false;
+      for (int i = 0; i < n_links; ++i)
+        masks = masks || p.links[i].diag != kNoDiag || p.links[i].kv_len % kAttnBN != 0;
+      usp_status_t st = D == 64 ? (masks ? launch_one<64, 4, true>(p, stream) : launch_one<64, 4, false>(p, stream))
+                                : (masks ? launch_one<128, 2, true>(p, stream) : launch_one<128, 2, false>(p, stream));
       if (st != USP_OK) return st;
       if (n_launched) ++*n_launched;
     }
