@@ -176,6 +176,10 @@ WORKLOADS = {
     "qwen_1328_u2r2": Workload("qwen_1328_u2r2", 1, 24, 128, 7145, 2, 2),
     "llm_64k_ring8_zigzag": Workload("llm_64k_ring8_zigzag", 1, 32, 128, 65536, 1, 8,
                                      causal=True, order="zigzag"),
+    # The long-context ring at a quarter of the length (16 half-chunks of 1024 rows), small enough
+    # for a full profiler capture of the attention kernel (402 MB of inputs, more than L2).
+    "llm_16k_ring8_zigzag": Workload("llm_16k_ring8_zigzag", 1, 32, 128, 16384, 1, 8,
+                                     causal=True, order="zigzag"),
     # Ring Anything / Ulysses Anything at large, uneven sizes: a sequence that no ring or head
     # count divides (zigzag half-chunks of 4111 and 4112 rows, not whole 128-row tiles), an uneven
     # stripe ring, and 24 heads over 5 Ulysses ranks (5/5/5/5/4 heads, 922/922/922/921/921 rows).
