@@ -301,6 +301,18 @@ usp_status_t usp_check_status(void* status, usp_stream_t stream);
 int usp_plan_pairs(int S, int ulysses_degree, int ring_degree, int causal, usp_order_t order,
                    int32_t* out, int cap);
 
+/* Host-only planning query for the fused ring (no device needed): the links usp_attention runs
+ * when the ring steps are fused, for B = 1, whichever mode the library would pick.  Writes up to
+ * `cap` records of 8 int32 each into `out`:
+ *   {ulysses index u, q ring chunk r, piece row0, piece rows, ring step k, kv ring chunk r2,
+ *    visible kv rows, diag}
+ * one per visible ring step of each piece of query rows; key c (0 <= c < visible kv rows, local to
+ * ring chunk r2) is visible to piece row i (0 <= i < piece rows, local row row0 + i of chunk r)
+ * iff c <= i + diag (diag = INT32_MAX: no causal limit).  Returns the total record count (which
+ * may exceed cap), or -1 on invalid arguments. */
+int usp_plan_chains(int S, int ulysses_degree, int ring_degree, int causal, usp_order_t order,
+                    int32_t* out, int cap);
+
 const char* usp_status_string(usp_status_t s);
 const char* usp_last_error(void);
 int usp_version(void); /* major*10000 + minor*100 + patch */

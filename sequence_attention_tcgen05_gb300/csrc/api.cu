@@ -1066,6 +1066,31 @@ int usp_plan_pairs(int S, int ulysses_degree, int ring_degree, int causal, usp_o
   return n;
 }
 
+int usp_plan_chains(int S, int ulysses_degree, int ring_degree, int causal, usp_order_t order,
+                    int32_t* out, int cap) {
+  Grid g;
+  if (build_grid(g, 1, S, std::max(1, ulysses_degree), 64, causal, ulysses_degree, ring_degree,
+                 order, nullptr, nullptr, USP_FP32) != USP_OK)
+    return -1;
+  AttnPlan pl;
+  if (plan_fused(g, 4, pl) != USP_OK) return -1;
+  int n = 0;
+  for (const AttnSeg& s : pl.segs) {
+    const int r = s.q_map / (3 * g.U), u = s.grp;
+    for (int i = 0; i < s.n_links; ++i) {
+      const AttnLink& lk = pl.links[s.link0 + i];
+      const int r2 = lk.k_map / (3 * g.U);
+      if (out && n < cap) {
+        int32_t* rec = out + 8 * n;
+        rec[0] = u; rec[1] = r; rec[2] = s.q_row0; rec[3] = s.q_len;
+        rec[4] = (r - r2 + g.R) % g.R; rec[5] = r2; rec[6] = lk.kv_len; rec[7] = lk.diag;
+      }
+      ++n;
+    }
+  }
+  return n;
+}
+
 const char* usp_status_string(usp_status_t s) {
   switch (s) {
     case USP_OK: return "ok";

@@ -24,7 +24,7 @@ EXPORTED = [
     "usp_attention_noalloc",
     "usp_attention_workspace_size", "usp_attention_ring_mode",
     "usp_check_status",
-    "usp_plan_pairs", "usp_status_string", "usp_last_error", "usp_version",
+    "usp_plan_pairs", "usp_plan_chains", "usp_status_string", "usp_last_error", "usp_version",
 ]
 
 
@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
         "usp_attention_ring_mode": [i32, i32, i32, i32, i32, i32, i32, i32, i32],
         "usp_check_status": [vp, vp],
         "usp_plan_pairs": [i32, i32, i32, i32, i32, i32p, i32],
+        "usp_plan_chains": [i32, i32, i32, i32, i32, i32p, i32],
         "usp_status_string": [i32],
         "usp_last_error": [],
         "usp_version": [],
@@ -290,6 +291,17 @@ def usp_plan_pairs(S, ulysses_degree, ring_degree, causal, order="contiguous"):
         raise UspError(USP_ERR_INVALID_ARG, "usp_plan_pairs", lib().usp_last_error().decode())
     buf = (ctypes.c_int32 * (8 * max(1, n)))()
     lib().usp_plan_pairs(S, ulysses_degree, ring_degree, int(causal), ORDERS[order], buf, n)
+    return [tuple(buf[8 * i: 8 * i + 8]) for i in range(n)]
+
+
+def usp_plan_chains(S, ulysses_degree, ring_degree, causal, order="contiguous"):
+    """The fused ring's links: (u, r, row0, rows, step, r2, kv_rows, diag) per visible ring step of
+    each piece of query rows."""
+    n = lib().usp_plan_chains(S, ulysses_degree, ring_degree, int(causal), ORDERS[order], None, 0)
+    if n < 0:
+        raise UspError(USP_ERR_INVALID_ARG, "usp_plan_chains", lib().usp_last_error().decode())
+    buf = (ctypes.c_int32 * (8 * max(1, n)))()
+    lib().usp_plan_chains(S, ulysses_degree, ring_degree, int(causal), ORDERS[order], buf, n)
     return [tuple(buf[8 * i: 8 * i + 8]) for i in range(n)]
 
 

@@ -182,6 +182,43 @@ def test_planner_matches_oracle_visibility(L, S, U, R, causal, order):
         assert at == len(pos[r])
 
 
+@pytest.mark.parametrize("S,U,R,causal,order", [
+    (65536, 1, 8, True, "zigzag"), (61, 1, 5, True, "zigzag"), (61, 1, 4, True, "stripe"),
+    (7145, 2, 2, False, "contiguous"), (47, 2, 3, True, "stripe"), (19, 1, 8, True, "contiguous"),
+    (5, 1, 8, True, "zigzag"), (1537, 1, 3, True, "zigzag"), (1000, 1, 3, False, "zigzag"),
+])
+def test_fused_chains_match_oracle_visibility(L, S, U, R, causal, order):
+    """The fused ring's pieces tile every ring chunk's query rows, each piece has at most one link
+    per ring step, in ring order, and for every row the links' visible keys are exactly the keys
+    of that ring step's chunk that the oracle's global positions allow."""
+    pos = oracle.ring_positions(order, S, R)
+    recs = usp.usp_plan_chains(S, U, R, causal, order)
+    pieces = {}
+    for (u, r, row0, rows, k, r2, kvlen, diag) in recs:
+        assert r2 == (r - k) % R
+        pieces.setdefault((u, r, row0, rows), []).append((k, r2, kvlen, diag))
+    for (u, r, row0, rows), links in pieces.items():
+        steps = [k for k, *_ in links]
+        assert steps == sorted(set(steps))  # ring order, each step once
+        qp = pos[r][row0:row0 + rows]
+        i = np.arange(rows)
+        got = {k: (np.full(rows, kvlen) if diag == INT32_MAX else np.clip(i + diag + 1, 0, kvlen))
+               for k, r2, kvlen, diag in links}
+        for k in range(R):
+            r2 = (r - k) % R
+            want = ((pos[r2][None, :] <= qp[:, None]).sum(axis=1) if causal
+                    else np.full(rows, len(pos[r2])))
+            assert np.array_equal(got.get(k, np.zeros(rows, dtype=int)), want), (u, r, row0, k)
+    for u in range(U):
+        for r in range(R):
+            spans = sorted((row0, rows) for (uu, rr, row0, rows) in pieces if uu == u and rr == r)
+            at = 0
+            for row0, rows in spans:
+                assert row0 == at
+                at += rows
+            assert at == len(pos[r])
+
+
 def test_planner_counts_every_causal_pair_once(L):
     """Across all ring steps, the planned runs see each causal (query, key) pair exactly once:
     sum over runs of the visible-key counts is S(S+1)/2, the count the FLOP figure uses."""
