@@ -216,3 +216,31 @@ def test_qkvpacked_matches_oracle(U, R, order, causal, mode, monkeypatch):
     ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), 1 / math.sqrt(D), causal)
     check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl,
                     f"qkvpacked U={U} R={R} {order} causal={causal} ring={mode}")
+
+
+@pytest.mark.parametrize("mode", ["fused", "separate"])
+@pytest.mark.parametrize("S,H,U,R,order,causal", [
+    (1, 2, 1, 8, "zigzag", True),       # one token, seven empty ring chunks
+    (5, 2, 1, 8, "zigzag", True),       # fewer tokens than half-chunks
+    (7, 3, 1, 16, "stripe", True),      # fewer tokens than ring ranks
+    (130, 4, 4, 4, "contiguous", True),  # 16 virtual ranks, one head each
+    (129, 4, 4, 4, "zigzag", False),
+    (2, 1, 1, 2, "contiguous", False),  # one query per rank
+])
+def test_degenerate_shapes(S, H, U, R, order, causal, mode, monkeypatch):
+    set_ring_mode(monkeypatch, mode)
+    o, l, (qb, kb, vb) = run_usp(1, S, H, 128, U, R, causal, order, seed=S)
+    ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), 1 / math.sqrt(128), causal)
+    check_attention(o, l, ro, rl, f"degenerate S={S} U={U} R={R} {order} causal={causal} ring={mode}")
+
+
+def test_largest_ring_256k_causal_zigzag():
+    """The largest ring the library runs (16 ranks) on a 256K-token causal sequence (8 heads of
+    128; 32 half-chunks of 8192 rows, addressed in place), fused ring steps: sampled rows of the
+    first and last heads against the oracle."""
+    w = synth.Workload("llm_256k_ring16_zigzag", 1, 8, 128, 262144, 1, 16, causal=True,
+                       order="zigzag")
+    assert usp.usp_attention_ring_mode(w.B, w.S, w.H, w.D, True, 1, 16, "zigzag",
+                                       usp.USP_FP32) == "fused"
+    rows = _sampled_rows(w, n=256)
+    _check_heads(w, [0, w.H - 1], rows)
