@@ -21,8 +21,9 @@
  *     only ([UAA]: the per-rank lengths travel on the host, which avoids forced device syncs).
  *   - Every call is asynchronous on `stream` (NULL = legacy default stream) and never
  *     synchronises the host with the device, except usp_check_status.
- *   - The library allocates no device memory and keeps no global state; calls on different
- *     streams are independent if their buffers are.
+ *   - The library allocates no device memory (usp_attention_noalloc's scratch is a static array
+ *     compiled into the library).  On the host it caches the plans of recent argument sets
+ *     (thread-safe); calls on different streams are independent if their buffers are.
  *   - Errors are return codes; usp_last_error() gives a thread-local message for the last
  *     failing call of the calling thread.  On any error nothing has been launched.
  *   - Head dimension D must be 64 or 128 for attention; re-layout accepts any D >= 1.

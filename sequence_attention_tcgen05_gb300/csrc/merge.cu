@@ -205,9 +205,9 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __rest
 }
 
 template <int NP>
-void launch_np(bool out_bf16, const MergeMap* map, unsigned blocks, cudaStream_t stream,
-               const float* o_parts, long long o_stride, const float* lse_parts,
-               long long lse_stride, long long n_vec, int D, void* o_out, float* lse_out) {
+void launch_np(bool out_bf16, const MergeMap* map, cudaStream_t stream, const float* o_parts,
+               long long o_stride, const float* lse_parts, long long lse_stride, long long n_vec,
+               int D, void* o_out, float* lse_out) {
   constexpr int U = NP <= 4 ? 2 : 1;  // 2: 48 registers, 5 CTAs per SM (4 measured slower: 72, 3)
   if (map) {
     long long rb = (map->row0[map->n_blocks] + 7) / 8;
@@ -240,7 +240,6 @@ void launch_np(bool out_bf16, const MergeMap* map, unsigned blocks, cudaStream_t
     kern<<<static_cast<unsigned>(ctas), 256, 0, stream>>>(o_parts, o_stride, lse_parts, lse_stride,
                                                           n_vec, D, o_out, lse_out);
   };
-  (void)blocks;
   if (out_bf16) go(lse_merge_kernel<NP, true, U>);
   else go(lse_merge_kernel<NP, false, U>);
 }
@@ -252,14 +251,9 @@ usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_
                               int D, void* o_out, bool out_bf16, float* lse_out,
                               const MergeMap* map, cudaStream_t stream) {
   if (n_vec == 0) return USP_OK;
-  const long long total = n_vec * (D / 4);
-  long long blocks = (total + 255) / 256;
-  const long long cap = static_cast<long long>(sm_count()) * 16;
-  if (blocks > cap) blocks = cap;
-  const unsigned nb = static_cast<unsigned>(blocks);
 #define USP_MERGE_CASE(N)                                                                        \
   case N:                                                                                        \
-    launch_np<N>(out_bf16, map, nb, stream, o_parts, o_part_stride, lse_parts, lse_part_stride,    \
+    launch_np<N>(out_bf16, map, stream, o_parts, o_part_stride, lse_parts, lse_part_stride,       \
                  n_vec, D, o_out, lse_out);                                                      \
     break;
   switch (n_parts) {
