@@ -21,6 +21,25 @@ int sm_count();               // SMs of the current device (cached per device; 1
 
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
+// Launch with programmatic stream serialization (for kernels that start with pdl_prologue()):
+// the kernel may be scheduled while the previous kernel of the stream finishes, which hides the
+// launch latency between back-to-back bandwidth-bound kernels.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Default split of n items over P parts: floor(n/P) + (p < n mod P).
 std::vector<int> default_split(int n, int P);
 

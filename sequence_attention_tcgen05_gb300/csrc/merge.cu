@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
                                                         long long lse_stride, long long n_vec,
                                                         int D, void* __restrict__ o_out,
                                                         float* __restrict__ lse_out) {
+  pdl_prologue();
   const int qpv = D >> 2;  // float4 per vector
   const long long total = n_vec * qpv;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __rest
                                                              float* __restrict__ lse_out,
                                                              const __grid_constant__ MergeMap m) {
   constexpr int kB = NP <= 2 ? 4 : (NP <= 4 ? 2 : 1);  // float4 slots per lane per batch
+  pdl_prologue();
   const int lane = threadIdx.x & 31;
   const long long total = m.row0[m.n_blocks];
   const long long step = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __rest
 }
 
 template <int NP>
-void launch_np(bool out_bf16, const MergeMap* map, cudaStream_t stream, const float* o_parts,
+cudaError_t launch_np(bool out_bf16, const MergeMap* map, cudaStream_t stream, const float* o_parts,
                long long o_stride, const float* lse_parts, long long lse_stride, long long n_vec,
                int D, void* o_out, float* lse_out) {
   constexpr int U = NP <= 4 ? 2 : 1;  // 2: 48 registers, 5 CTAs per SM (4 measured slower: 72, 3)
@@ -215,16 +217,12 @@ void launch_np(bool out_bf16, const MergeMap* map, cudaStream_t stream, const fl
     if (rb > cap) rb = cap;
     const unsigned nb = static_cast<unsigned>(std::max(1LL, rb));
     auto go = [&](auto kern) {
-      kern<<<nb, 256, 0, stream>>>(o_parts, o_stride, lse_parts, lse_stride, D, o_out, lse_out, *map);
+      return launch_pdl(kern, dim3(nb), dim3(256), 0, stream, o_parts, o_stride, lse_parts,
+                        lse_stride, D, o_out, lse_out, *map);
     };
-    if (map->all_seen) {
-      if (out_bf16) go(lse_merge_rows_kernel<NP, true, true>);
-      else go(lse_merge_rows_kernel<NP, false, true>);
-    } else {
-      if (out_bf16) go(lse_merge_rows_kernel<NP, true, false>);
-      else go(lse_merge_rows_kernel<NP, false, false>);
-    }
-    return;
+    if (map->all_seen)
+      return out_bf16 ? go(lse_merge_rows_kernel<NP, true, true>) : go(lse_merge_rows_kernel<NP, false, true>);
+    return out_bf16 ? go(lse_merge_rows_kernel<NP, true, false>) : go(lse_merge_rows_kernel<NP, false, false>);
   }
   // persistent grid: the CTAs that fit on the GPU at once (each thread then takes an equal share of
   // the float4 slots, U at a time), never more threads than slots need
@@ -237,11 +235,10 @@ void launch_np(bool out_bf16, const MergeMap* map, cudaStream_t stream, const fl
     const long long slots = n_vec * (D / 4);
     const long long need = (slots + 256LL * U - 1) / (256LL * U);
     const long long ctas = std::max(1LL, std::min<long long>(static_cast<long long>(per_sm) * sm_count(), need));
-    kern<<<static_cast<unsigned>(ctas), 256, 0, stream>>>(o_parts, o_stride, lse_parts, lse_stride,
-                                                          n_vec, D, o_out, lse_out);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(256), 0, stream, o_parts,
+                      o_stride, lse_parts, lse_stride, n_vec, D, o_out, lse_out);
   };
-  if (out_bf16) go(lse_merge_kernel<NP, true, U>);
-  else go(lse_merge_kernel<NP, false, U>);
+  return out_bf16 ? go(lse_merge_kernel<NP, true, U>) : go(lse_merge_kernel<NP, false, U>);
 }
 
 }  // namespace
@@ -251,10 +248,11 @@ usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_
                               int D, void* o_out, bool out_bf16, float* lse_out,
                               const MergeMap* map, cudaStream_t stream) {
   if (n_vec == 0) return USP_OK;
+  cudaError_t e = cudaSuccess;
 #define USP_MERGE_CASE(N)                                                                        \
   case N:                                                                                        \
-    launch_np<N>(out_bf16, map, stream, o_parts, o_part_stride, lse_parts, lse_part_stride,       \
-                 n_vec, D, o_out, lse_out);                                                      \
+    e = launch_np<N>(out_bf16, map, stream, o_parts, o_part_stride, lse_parts, lse_part_stride,   \
+                     n_vec, D, o_out, lse_out);                                                  \
     break;
   switch (n_parts) {
     USP_MERGE_CASE(1) USP_MERGE_CASE(2) USP_MERGE_CASE(3) USP_MERGE_CASE(4) USP_MERGE_CASE(5)
@@ -265,6 +263,7 @@ usp_status_t launch_lse_merge(int n_parts, const float* o_parts, int64_t o_part_
       return fail(USP_ERR_INVALID_ARG, "n_parts %d outside [1, 16]", n_parts);
   }
 #undef USP_MERGE_CASE
+  if (e != cudaSuccess) return fail(USP_ERR_CUDA, "lse merge kernel: %s", cudaGetErrorString(e));
   return check_launch("lse merge kernel");
 }
 

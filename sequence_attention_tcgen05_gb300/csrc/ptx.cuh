@@ -105,6 +105,15 @@ __device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Programmatic dependent launch, kernel side: let the next kernel of the stream be scheduled once
+// every CTA of this one has started, then wait until the previous kernel has completed and its
+// memory is visible (a no-op when the kernel was launched without the programmatic attribute).
+// Call before the kernel's first global memory access.
+__device__ __forceinline__ void pdl_prologue() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // tcgen05
 // ---------------------------------------------------------------------------------------------

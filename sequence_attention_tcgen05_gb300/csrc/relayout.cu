@@ -13,6 +13,7 @@
 #include <cstdio>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace usp {
 namespace {
@@ -74,6 +75,7 @@ template <int VEC>
 __global__ void __launch_bounds__(256) relayout_block_kernel(const __grid_constant__ RelayoutParams p,
                                                              long long n_blocks) {
   using T = typename Vec<VEC>::T;
+  pdl_prologue();
   const int lane = threadIdx.x & 31;
   const long long rows = p.row0[p.R];
   const long long per_tensor = rows * p.U;
@@ -113,6 +115,7 @@ template <int VEC>
 __global__ void __launch_bounds__(256) relayout_small_kernel(const __grid_constant__ RelayoutParams p) {
   using T = typename Vec<VEC>::T;
   constexpr int kBatch = 8;
+  pdl_prologue();
   const char* __restrict__ src = p.src[blockIdx.y];
   char* __restrict__ dst = p.dst[blockIdx.y];
   const long long total = p.row0[p.R];
@@ -172,12 +175,14 @@ usp_status_t launch_relayout(RelayoutParams& p, cudaStream_t stream) {
     long long blocks = (total + 255) / 256;
     if (blocks > sms * 16) blocks = sms * 16;
     dim3 grid(static_cast<unsigned>(blocks), p.n_tensors);
+    cudaError_t e;
     switch (g) {
-      case 16: relayout_small_kernel<16><<<grid, 256, 0, stream>>>(p); break;
-      case 8: relayout_small_kernel<8><<<grid, 256, 0, stream>>>(p); break;
-      case 4: relayout_small_kernel<4><<<grid, 256, 0, stream>>>(p); break;
-      default: relayout_small_kernel<2><<<grid, 256, 0, stream>>>(p); break;
+      case 16: e = launch_pdl(relayout_small_kernel<16>, grid, dim3(256), 0, stream, p); break;
+      case 8: e = launch_pdl(relayout_small_kernel<8>, grid, dim3(256), 0, stream, p); break;
+      case 4: e = launch_pdl(relayout_small_kernel<4>, grid, dim3(256), 0, stream, p); break;
+      default: e = launch_pdl(relayout_small_kernel<2>, grid, dim3(256), 0, stream, p); break;
     }
+    if (e != cudaSuccess) return fail(USP_ERR_CUDA, "relayout kernel: %s", cudaGetErrorString(e));
     return check_launch("relayout kernel");
   }
   // one warp per (tensor, row, head group) block, 8 warps per CTA; the hardware hands CTAs to the
@@ -186,12 +191,14 @@ usp_status_t launch_relayout(RelayoutParams& p, cudaStream_t stream) {
   long long ctas = (n_blocks + 7) / 8;
   if (ctas > (1LL << 24)) ctas = 1LL << 24;
   const unsigned grid = static_cast<unsigned>(ctas);
+  cudaError_t e;
   switch (g) {
-    case 16: relayout_block_kernel<16><<<grid, 256, 0, stream>>>(p, n_blocks); break;
-    case 8: relayout_block_kernel<8><<<grid, 256, 0, stream>>>(p, n_blocks); break;
-    case 4: relayout_block_kernel<4><<<grid, 256, 0, stream>>>(p, n_blocks); break;
-    default: relayout_block_kernel<2><<<grid, 256, 0, stream>>>(p, n_blocks); break;
+    case 16: e = launch_pdl(relayout_block_kernel<16>, dim3(grid), dim3(256), 0, stream, p, n_blocks); break;
+    case 8: e = launch_pdl(relayout_block_kernel<8>, dim3(grid), dim3(256), 0, stream, p, n_blocks); break;
+    case 4: e = launch_pdl(relayout_block_kernel<4>, dim3(grid), dim3(256), 0, stream, p, n_blocks); break;
+    default: e = launch_pdl(relayout_block_kernel<2>, dim3(grid), dim3(256), 0, stream, p, n_blocks); break;
   }
+  if (e != cudaSuccess) return fail(USP_ERR_CUDA, "relayout kernel: %s", cudaGetErrorString(e));
   return check_launch("relayout kernel");
 }
 
