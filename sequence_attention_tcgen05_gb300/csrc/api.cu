@@ -239,6 +239,14 @@ struct Grid {
 
 bool choose_fused_ring(const Grid& g, usp_dtype_t o_dt);
 
+// USP_RING_MERGE (environment, read at each call): 1 = "fused", 2 = "separate", 0 = unset/other.
+int ring_env() {
+  const char* env = std::getenv("USP_RING_MERGE");
+  if (env && std::strcmp(env, "fused") == 0) return 1;
+  if (env && std::strcmp(env, "separate") == 0) return 2;
+  return 0;
+}
+
 usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int causal, int U, int R,
                         usp_order_t order, const int32_t* seq_lens, const int32_t* head_counts,
                         usp_dtype_t o_dt) {
@@ -480,9 +488,7 @@ double launch_periods(std::vector<AttnSeg> segs, const std::vector<AttnLink>& li
 // query), so usp_attention_workspace_size and usp_attention agree.  USP_RING_MERGE=fused or
 // =separate (environment, read at each call) overrides the model.
 bool choose_fused_ring(const Grid& g, usp_dtype_t o_dt) {
-  const char* env = std::getenv("USP_RING_MERGE");
-  if (env && std::strcmp(env, "fused") == 0) return true;
-  if (env && std::strcmp(env, "separate") == 0) return false;
+  if (const int env = ring_env()) return env == 1;
   constexpr int kModelCtas = 152;
   constexpr double kPeriodBytes = 6.0e12 * 1.55e-6;  // merge bytes per key-tile period
   AttnPlan sep, fus;
@@ -530,13 +536,6 @@ struct PlanEntry {
 constexpr size_t kPlanCache = 16;
 std::mutex g_plan_mu;
 std::vector<std::shared_ptr<const PlanEntry>> g_plan_cache;  // most recent first
-
-int ring_env() {
-  const char* env = std::getenv("USP_RING_MERGE");
-  if (env && std::strcmp(env, "fused") == 0) return 1;
-  if (env && std::strcmp(env, "separate") == 0) return 2;
-  return 0;
-}
 
 // The validated grid and attention plan for these arguments (built and cached on first use).
 usp_status_t get_plan(int B, int S, int H, int D, int causal, int U, int R, usp_order_t order,
