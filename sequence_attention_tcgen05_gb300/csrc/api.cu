@@ -878,68 +878,93 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
 
   // 2. attention over every (Ulysses rank, q ring chunk, ring step) pair in one launch: one
   //    segment per chunk pair (ring partials or, with one ring rank, the final output), or one
-  //    chain per piece of query rows across all ring steps (fused ring: the final output)
-  static thread_local AttnParams params;
-  AttnParams& p = params;
-  std::memset(&p, 0, sizeof(p));
-  for (int r = 0; r < R; ++r) {
-    for (int u = 0; u < U; ++u) {
-      const void* base[3];
-      int64_t row_stride, batch_stride;
-      int64_t piece_rows = std::max(1, g.S_r[r]), piece_stride = 0;
-      int n_pieces = 1;
-      if (g.fused_in) {
-        const int64_t e0 = int64_t(g.pos[r].start[0]) * in_rs + int64_t(g.hoff[u]) * D;
-        base[0] = static_cast<const uint16_t*>(q) + e0;
-        base[1] = static_cast<const uint16_t*>(k) + e0;
-        base[2] = static_cast<const uint16_t*>(v) + e0;
-        row_stride = int64_t(g.pos[r].stride) * in_rs;
-        batch_stride = int64_t(S) * in_rs;
-        if (two_pieces(g.pos[r])) {  // zigzag chunk: its two half-chunks
-          piece_rows = g.pos[r].len[0];
-          n_pieces = 2;
-          piece_stride = int64_t(g.pos[r].start[1] - g.pos[r].start[0]) * in_rs;
-        }
-      } else {
-        const int64_t off = g.woff(r, u, D) * 2;
-        base[0] = ws + g.off_q + off;
-        base[1] = ws + g.off_k + off;
-        base[2] = ws + g.off_v + off;
-        row_stride = int64_t(g.h[u]) * D;
-        batch_stride = int64_t(g.S_r[r]) * row_stride;
-      }
-      if (B == 1) batch_stride = std::max<int64_t>(1, g.S_r[r]) * row_stride;
-      for (int t = 0; t < 3; ++t) {
-        const int mi = map_index(g, r, u, t);
-        if ((st = make_qkv_map(&p.maps[mi], base[t], g.h[u], D, piece_rows, n_pieces, B, row_stride,
-                               piece_stride, batch_stride)))
-          return st;
-        p.map_rows[mi] = n_pieces > 1 ? static_cast<int>(piece_rows) : 0;
-      }
-    }
-  }
-  p.B = B;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.status = reinterpret_cast<uint32_t*>(ws);
-  p.budget_ns = wait_budget_ns();
-  p.withhold_loads = withhold_loads();
+  //    chain per piece of query rows across all ring steps (fused ring: the final output).
+  //    A thread that repeats its previous call (same plan, buffers and settings) relaunches the
+  //    parameters it built then, without encoding the tensor maps again.
+  struct CallMemo {
+    std::shared_ptr<const PlanEntry> pe;
+    const void *q, *k, *v, *o, *lse, *ws;
+    int64_t in_rs;
+    float scale;
+    unsigned long long budget;
+    int withhold;
+    std::vector<AttnLaunch> launches;
+  };
+  static thread_local CallMemo memo;
+  const unsigned long long budget = wait_budget_ns();
+  const int withhold = withhold_loads();
   const bool partials = R > 1 && !g.fused_ring;
-  p.o_bf16 = partials ? 0 : (o_dt == USP_BF16);
-  // the cached plan's segments, bound to this call's output and workspace
-  std::vector<AttnSeg> segs = pe->plan.segs;
-  for (size_t i = 0; i < segs.size(); ++i) {
-    const SegOut& so = pe->plan.outs[i];
-    if (so.partial) {
-      segs[i].o = ws + so.o_off;
-      segs[i].lse = reinterpret_cast<float*>(ws + so.lse_off);
-    } else {
-      segs[i].o = static_cast<char*>(o) + so.o_off;
-      segs[i].lse = lse ? reinterpret_cast<float*>(reinterpret_cast<char*>(lse) + so.lse_off) : nullptr;
+  if (memo.pe == pe && memo.q == q && memo.k == k && memo.v == v && memo.o == o && memo.lse == lse &&
+      memo.ws == workspace && memo.in_rs == in_rs && memo.scale == scale && memo.budget == budget &&
+      memo.withhold == withhold) {
+    if ((st = run_attention(memo.launches, D, stream))) return st;
+    n_launch[1] = static_cast<int>(memo.launches.size());
+  } else {
+    memo.pe.reset();
+    static thread_local AttnParams params;
+    AttnParams& p = params;
+    std::memset(&p, 0, sizeof(p));
+    for (int r = 0; r < R; ++r) {
+      for (int u = 0; u < U; ++u) {
+        const void* base[3];
+        int64_t row_stride, batch_stride;
+        int64_t piece_rows = std::max(1, g.S_r[r]), piece_stride = 0;
+        int n_pieces = 1;
+        if (g.fused_in) {
+          const int64_t e0 = int64_t(g.pos[r].start[0]) * in_rs + int64_t(g.hoff[u]) * D;
+          base[0] = static_cast<const uint16_t*>(q) + e0;
+          base[1] = static_cast<const uint16_t*>(k) + e0;
+          base[2] = static_cast<const uint16_t*>(v) + e0;
+          row_stride = int64_t(g.pos[r].stride) * in_rs;
+          batch_stride = int64_t(S) * in_rs;
+          if (two_pieces(g.pos[r])) {  // zigzag chunk: its two half-chunks
+            piece_rows = g.pos[r].len[0];
+            n_pieces = 2;
+            piece_stride = int64_t(g.pos[r].start[1] - g.pos[r].start[0]) * in_rs;
+          }
+        } else {
+          const int64_t off = g.woff(r, u, D) * 2;
+          base[0] = ws + g.off_q + off;
+          base[1] = ws + g.off_k + off;
+          base[2] = ws + g.off_v + off;
+          row_stride = int64_t(g.h[u]) * D;
+          batch_stride = int64_t(g.S_r[r]) * row_stride;
+        }
+        if (B == 1) batch_stride = std::max<int64_t>(1, g.S_r[r]) * row_stride;
+        for (int t = 0; t < 3; ++t) {
+          const int mi = map_index(g, r, u, t);
+          if ((st = make_qkv_map(&p.maps[mi], base[t], g.h[u], D, piece_rows, n_pieces, B, row_stride,
+                                 piece_stride, batch_stride)))
+            return st;
+          p.map_rows[mi] = n_pieces > 1 ? static_cast<int>(piece_rows) : 0;
+        }
+      }
     }
+    p.B = B;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.status = reinterpret_cast<uint32_t*>(ws);
+    p.budget_ns = budget;
+    p.withhold_loads = withhold;
+    p.o_bf16 = partials ? 0 : (o_dt == USP_BF16);
+    // the cached plan's segments, bound to this call's output and workspace
+    std::vector<AttnSeg> segs = pe->plan.segs;
+    for (size_t i = 0; i < segs.size(); ++i) {
+      const SegOut& so = pe->plan.outs[i];
+      if (so.partial) {
+        segs[i].o = ws + so.o_off;
+        segs[i].lse = reinterpret_cast<float*>(ws + so.lse_off);
+      } else {
+        segs[i].o = static_cast<char*>(o) + so.o_off;
+        segs[i].lse = lse ? reinterpret_cast<float*>(reinterpret_cast<char*>(lse) + so.lse_off) : nullptr;
+      }
+    }
+    if ((st = pack_attention(p, segs, pe->plan.links, memo.launches))) return st;
+    memo.pe = pe;
+    memo.q = q; memo.k = k; memo.v = v; memo.o = o; memo.lse = lse; memo.ws = workspace;
+    memo.in_rs = in_rs; memo.scale = scale; memo.budget = budget; memo.withhold = withhold;
+    if ((st = run_attention(memo.launches, D, stream))) return st;
+    n_launch[1] = static_cast<int>(memo.launches.size());
   }
-  int n_att = 0;
-  if ((st = launch_attention(p, segs, pe->plan.links, D, stream, &n_att))) return st;
-  n_launch[1] = n_att;
   if ((st = mark(2))) return st;
 
   // 3. merge the ring partials straight into the global layout (the head -> seq all-to-all and the

@@ -744,11 +744,10 @@ usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D
   return USP_OK;
 }
 
-usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs,
-                              const std::vector<AttnLink>& links, int D, cudaStream_t stream,
-                              int* n_launched) {
-  if (n_launched) *n_launched = 0;
-  if (!(p.scale_log2 > 0.f)) return fail(USP_ERR_INVALID_ARG, "the softmax scale must be positive");
+usp_status_t pack_attention(const AttnParams& base, std::vector<AttnSeg>& segs,
+                            const std::vector<AttnLink>& links, std::vector<AttnLaunch>& out) {
+  out.clear();
+  if (!(base.scale_log2 > 0.f)) return fail(USP_ERR_INVALID_ARG, "the softmax scale must be positive");
   // Segments grouped by unit group, longest first within a group: sort by the key tiles their
   // longest query block visits.
   auto cost = [&](const AttnSeg& s) {
@@ -761,6 +760,10 @@ usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs,
   });
   size_t at = 0;
   while (at < segs.size()) {
+    out.emplace_back();
+    AttnLaunch& L = out.back();
+    L.params = base;
+    AttnParams& p = L.params;
     long long units = 0;
     int used = 0, n_links = 0, n_groups = 0;
     for (; at < segs.size() && used < kAttnMaxSegs; ++at) {
@@ -795,17 +798,33 @@ usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs,
     p.n_segs = used;
     p.n_groups = n_groups;
     p.n_units = static_cast<int>(units);
-    if (units > 0) {
-      // the mask-free kernel when every link is whole key tiles without a causal diagonal
-      bool masks = false;
-      for (int i = 0; i < n_links; ++i)
-        masks = masks || p.links[i].diag != kNoDiag || p.links[i].kv_len % kAttnBN != 0;
-      usp_status_t st = D == 64 ? (masks ? launch_one<64, 4, true>(p, stream) : launch_one<64, 4, false>(p, stream))
-                                : (masks ? launch_one<128, 2, true>(p, stream) : launch_one<128, 2, false>(p, stream));
-      if (st != USP_OK) return st;
-      if (n_launched) ++*n_launched;
-    }
+    // the mask-free kernel when every link is whole key tiles without a causal diagonal
+    L.masks = false;
+    for (int i = 0; i < n_links; ++i)
+      L.masks = L.masks || p.links[i].diag != kNoDiag || p.links[i].kv_len % kAttnBN != 0;
+    if (units == 0) out.pop_back();
   }
+  return USP_OK;
+}
+
+usp_status_t run_attention(const std::vector<AttnLaunch>& launches, int D, cudaStream_t stream) {
+  for (const AttnLaunch& L : launches) {
+    const AttnParams& p = L.params;
+    usp_status_t st = D == 64 ? (L.masks ? launch_one<64, 4, true>(p, stream) : launch_one<64, 4, false>(p, stream))
+                              : (L.masks ? launch_one<128, 2, true>(p, stream) : launch_one<128, 2, false>(p, stream));
+    if (st != USP_OK) return st;
+  }
+  return USP_OK;
+}
+
+usp_status_t launch_attention(AttnParams& p, std::vector<AttnSeg>& segs,
+                              const std::vector<AttnLink>& links, int D, cudaStream_t stream,
+                              int* n_launched) {
+  if (n_launched) *n_launched = 0;
+  static thread_local std::vector<AttnLaunch> launches;
+  if (usp_status_t st = pack_attention(p, segs, links, launches)) return st;
+  if (usp_status_t st = run_attention(launches, D, stream)) return st;
+  if (n_launched) *n_launched = static_cast<int>(launches.size());
   return USP_OK;
 }
 

@@ -203,6 +203,18 @@ usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D
                           int n_pieces, int B, int64_t row_stride, int64_t piece_stride,
                           int64_t batch_stride);
 
+// One kernel launch's parameters (segments, links and groups packed) and which instantiation runs
+// it (masks = false: no link needs a mask).
+struct AttnLaunch {
+  AttnParams params;
+  bool masks;
+};
+// Packs the segments (sorted in place) and their links into launches, each starting from `base`
+// (maps, scale, status, budget); then runs them.
+usp_status_t pack_attention(const AttnParams& base, std::vector<AttnSeg>& segs,
+                            const std::vector<AttnLink>& links, std::vector<AttnLaunch>& out);
+usp_status_t run_attention(const std::vector<AttnLaunch>& launches, int D, cudaStream_t stream);
+
 // Launch over all segments, each with its own links (split into several launches if there are
 // more than fit; `n_launched`, if not null, receives how many).  The links of segs[i] are
 // links[segs[i].link0 .. + n_links) of `links`.

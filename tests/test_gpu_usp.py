@@ -244,3 +244,27 @@ def test_largest_ring_256k_causal_zigzag():
                                        usp.USP_FP32) == "fused"
     rows = _sampled_rows(w, n=256)
     _check_heads(w, [0, w.H - 1], rows)
+
+
+def test_repeated_calls_on_the_same_buffers(monkeypatch):
+    """A call that repeats the previous one (same shapes, buffers and settings) relaunches the
+    kernel parameters built then: new input contents in the same buffers must still give the right
+    result, and a changed ring-mode override must not reuse them."""
+    t = torch()
+    B, S, H, D, U, R = 1, 1537, 4, 128, 2, 3
+    scale = 1 / math.sqrt(D)
+    q, k, v = (t.empty((B, S, H, D), dtype=t.bfloat16, device="cuda") for _ in range(3))
+    o = t.empty((B, S, H, D), dtype=t.float32, device="cuda")
+    lse = t.empty((B, S, H), dtype=t.float32, device="cuda")
+    monkeypatch.setenv("USP_RING_MERGE", "separate")  # the larger workspace of the two modes
+    nbytes = usp.usp_attention_workspace_size(B, S, H, D, U, R, "zigzag", usp.USP_FP32, True)
+    ws = t.zeros(nbytes, dtype=t.uint8, device="cuda")
+    for seed, mode in ((1, "separate"), (2, "separate"), (3, "fused"), (4, "fused")):
+        monkeypatch.setenv("USP_RING_MERGE", mode)
+        qb, kb, vb = synth.make_qkv_bits(B, S, H, D, seed)
+        for dst, bits in zip((q, k, v), (qb, kb, vb)):
+            dst.copy_(to_dev_bf16(bits))
+        usp.usp_attention(q, k, v, B, S, H, D, scale, True, U, R, o, lse, ws, nbytes, order="zigzag")
+        assert usp.usp_check_status(ws) == usp.USP_OK
+        ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), scale, True)
+        check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl, f"repeat seed={seed} ring={mode}")
