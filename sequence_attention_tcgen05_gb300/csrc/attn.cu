@@ -43,7 +43,9 @@
 //                max exceeds it by more than 8 (log2 units), its part of O rescaled in TMEM and
 //                the exponentials redone.  P stays bounded by 2^16, and the stale m is exact after
 //                the final division by the row sum.  Epilogue: O / l (fp32 or bf16) and
-//                lse = (m + log2 l) ln 2 stored from the same fragments.
+//                lse = (m + log2 l) ln 2 from the same fragments; bf16 O words are first
+//                transposed across the four threads of each row (two shuffle rounds), so that
+//                each thread writes whole 8-column groups as 16-byte stores.
 // Without a max exchange between the warpgroups the softmax term of the chain
 // S_x(j) -> softmax -> O_x += P V -> S_x(j+1), which sets the kernel's period per key tile, is
 // one warpgroup's own work.
@@ -195,6 +197,24 @@ __device__ __forceinline__ void exp_tile(const uint32_t (&r)[64], uint64_t c2, f
     float s0, s1;
     f2_unpack(acc[i], s0, s1);
     sum[i] = s0 + s1;
+  }
+}
+
+// 4 x 4 transpose of 32-bit words across the four threads of a row (lanes 4r .. 4r+3): on entry
+// thread c holds w[j] = its word of group j, on return w[j] = thread j's word of group c.  Two
+// butterfly rounds; in each, a thread keeps the words whose index bit matches its lane bit and
+// trades the other with its partner.
+__device__ __forceinline__ void quad_transpose4(uint32_t* w, int lane) {
+#pragma unroll
+  for (int bit = 1; bit <= 2; bit <<= 1) {
+    const bool hi = (lane & bit) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j & bit) continue;
+      const uint32_t send = hi ? w[j] : w[j + bit];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, bit);
+      if (hi) w[j] = recv; else w[j + bit] = recv;
+    }
   }
 }
 
@@ -656,16 +676,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tc_fence_before();
           mbar_arrive(&o_empty[x]);
         }
+        if (p.o_bf16) {
+          // The four threads of a row hold one bf16 pair of each 8-column group; a 4 x 4 word
+          // transpose across them (two shuffle rounds) gives thread lane%4 all of groups
+          // 4g + lane%4, which it writes as one 16-byte store per group.
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (!row_valid_at(i)) continue;
+          for (int i = 0; i < 2; ++i) {
+            uint32_t w[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float v0 = __uint_as_float(o[4 * k + 2 * i]) * inv_l[i];
-            const float v1 = __uint_as_float(o[4 * k + 2 * i + 1]) * inv_l[i];
-            const long long at = o_elem[i] + cc * 64 + 8 * k + cq;
-            if (p.o_bf16) reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(s.o) + at)[0] = pack_bf16x2(v0, v1);
-            else reinterpret_cast<float2*>(static_cast<float*>(s.o) + at)[0] = make_float2(v0, v1);
+            for (int k = 0; k < 8; ++k)
+              w[k] = pack_bf16x2(__uint_as_float(o[4 * k + 2 * i]) * inv_l[i],
+                                 __uint_as_float(o[4 * k + 2 * i + 1]) * inv_l[i]);
+            quad_transpose4(w, lane);
+            quad_transpose4(w + 4, lane);
+            if (row_valid_at(i)) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.o) + o_elem[i] + cc * 64 +
+                                                    4 * cq);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);  // group lane%4
+              dst[4] = make_uint4(w[4], w[5], w[6], w[7]);  // group 4 + lane%4
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (!row_valid_at(i)) continue;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float v0 = __uint_as_float(o[4 * k + 2 * i]) * inv_l[i];
+              const float v1 = __uint_as_float(o[4 * k + 2 * i + 1]) * inv_l[i];
+              reinterpret_cast<float2*>(static_cast<float*>(s.o) + o_elem[i] + cc * 64 + 8 * k + cq)[0] =
+                  make_float2(v0, v1);
+            }
           }
         }
       }

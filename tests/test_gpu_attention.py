@@ -100,6 +100,23 @@ def test_bf16_output_and_packed_qkv():
     check_attention(o, l, ro, rl, "bf16 packed")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("B,H,Sq,Sk,causal", [
+    (1, 1, 1, 1, False), (2, 3, 131, 200, False), (1, 2, 300, 129, False), (1, 5, 517, 700, False),
+    (2, 2, 300, 300, True), (1, 3, 133, 133, True)])
+def test_bf16_output_every_element(B, H, Sq, Sk, D, causal):
+    """bf16 O is written as 16-byte stores after a word transpose across the four threads of each
+    row: every element of every valid row must be written (an element left at the canary fill
+    fails the comparison) and nothing around the buffer touched, for ragged row counts."""
+    spec = (([(0, Sq)], 1), ([(0, Sk)], 1)) if causal else (None, None)
+    o, l, q, k, v, scale = run_partial(B, H, Sq, Sk, D, spec[0], spec[1], seed=11, out="bf16")
+    if causal:
+        ro, rl = oracle.attention(q, k, v, scale, True, positions(spec[0]), positions(spec[1]))
+    else:
+        ro, rl = oracle.attention(q, k, v, scale)
+    check_attention(o, l, ro, rl, f"bf16 out {B},{H},{Sq},{Sk},{D} causal={causal}")
+
+
 def test_repeat_calls_identical():
     a = run_partial(1, 4, 640, 900, 128, seed=9)
     b = run_partial(1, 4, 640, 900, 128, seed=9)
