@@ -18,7 +18,10 @@ loop whose events sit between the phases.  Times come from CUDA events on the la
             copies Q, K, V host->device, runs usp_attention and copies O and LSE back.  `value` is
             pipelined as a caller serving a stream of requests runs it (two device buffer sets;
             step i's copy-in overlaps step i-1's attention and copy-out); `serial_value` runs one
-            step at a time on one stream.
+            step at a time on one stream.  `host_link` = the copies' rates in this run (each
+            direction alone and both at once), `pipelined_estimate` = the pipelined figure they
+            predict (the host link is shared with other jobs, so it varies from run to run), and
+            `serial_stage_ms` / `pipelined_stage_ms` = each stage's median time.
   roofline  the partial-attention phase alone against the measured dense bf16 tensor peak.
   relayout_merge  GB/s of the step's bandwidth-bound phases, plus separately timed standalone
             measurements of the re-layout entry points on the workload's tensors and of the LSE
@@ -56,8 +59,8 @@ NOMINAL_HBM_GBS = 8000.0
 # dram__bytes_write.sum from one ncu capture of that workload's launch, with the hash of the kernel
 # sources they were taken on; reported as null once the kernel changes.
 ATTN_TRAFFIC = {
-    # one full-size launch: dram__bytes_read.sum 3854501376 + dram__bytes_write.sum 574109952
-    "llm_64k_ring8_zigzag": {"bytes": 3854501376 + 574109952, "kernel_hash": "b1ed7830221165e0"},
+    # one full-size launch: dram__bytes_read.sum 3624078848 + dram__bytes_write.sum 574117376
+    "llm_64k_ring8_zigzag": {"bytes": 3624078848 + 574117376, "kernel_hash": "a284d9bfa3308ac0"},
 }
 L2_BYTES = 129e6
 
@@ -287,6 +290,51 @@ def back_to_back_us(launch, n_sets: int, reps: int, flush, stream):
             break
         head_us = 2.0 * host_us + 100.0  # the host fell behind the GPU: repeat with a longer spin
     return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def host_link_rates(dev_in, host_in, dev_out, host_out, stream, reps: int = 3):
+    """Median ms and GB/s of one step's host->device copies alone, its device->host copies alone,
+    and both on two streams at once (the host link is shared by the two directions)."""
+    import torch
+    n_in = sum(t.numel() * t.element_size() for t in dev_in)
+    n_out = sum(t.numel() * t.element_size() for t in dev_out)
+    s2 = torch.cuda.Stream(stream.device)
+
+    def copy_in(s):
+        with torch.cuda.stream(s):
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+
+    def copy_out(s):
+        with torch.cuda.stream(s):
+            for h, d in zip(host_out, dev_out):
+                h.copy_(d, non_blocking=True)
+
+    def both(s):
+        start = torch.cuda.Event()
+        start.record(s)
+        s2.wait_event(start)
+        copy_in(s)
+        copy_out(s2)
+        done = torch.cuda.Event()
+        done.record(s2)
+        s.wait_event(done)
+
+    def median_ms(fn):
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(stream)
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    t_in, t_out, t_both = median_ms(copy_in), median_ms(copy_out), median_ms(both)
+    return {"h2d_ms": t_in, "h2d_GB/s": n_in / t_in / 1e6, "d2h_ms": t_out,
+            "d2h_GB/s": n_out / t_out / 1e6, "both_ms": t_both,
+            "both_GB/s": (n_in + n_out) / t_both / 1e6}
 
 
 def rotation(bytes_per_set: float) -> int:
@@ -652,23 +700,32 @@ def run_ours(args):
     e2e_steps = max(3, min(args.steps, 50))
     o_host = torch.empty(o.shape, dtype=out_dt).pin_memory()
     l_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    # (a) serial: one step at a time on one stream (copy in, usp_attention, copy out)
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # (a) serial: one step at a time on one stream (copy in, usp_attention, copy out), with an
+    # event between the stages
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     e2e_ms = 0.0
+    serial_stages = {"h2d": [], "attention": [], "d2h": []}
     for i in range(e2e_steps + 1):
         flush()
-        e_start.record(stream)
+        ev_s[0].record(stream)
         for dst, src in zip((q, k, v), host):
             dst.copy_(src, non_blocking=True)
+        ev_s[1].record(stream)
         usp.usp_attention(q, k, v, B, S, H, D, scale, w.causal, w.ulysses_degree, w.ring_degree,
                           o, lse, ws, nbytes, seq, None, w.order, o_code, stream)
+        ev_s[2].record(stream)
         o_host.copy_(o, non_blocking=True)
         l_host.copy_(lse, non_blocking=True)
-        e_end.record(stream)
-        e_end.synchronize()
+        ev_s[3].record(stream)
+        ev_s[3].synchronize()
         if i > 0:
-            e2e_ms += e_start.elapsed_time(e_end)
+            e2e_ms += ev_s[0].elapsed_time(ev_s[3])
+            for n, a, b_ in (("h2d", 0, 1), ("attention", 1, 2), ("d2h", 2, 3)):
+                serial_stages[n].append(ev_s[a].elapsed_time(ev_s[b_]))
     e2e_serial, _ = aggregate(e2e_steps * flops, e2e_ms / 1000.0, world, device)
+    # the host link's rates in this run (the e2e figure's ceiling): each direction alone, then both
+    # at once, as the pipelined loop runs them
+    link = host_link_rates((q, k, v), host, (o, lse), (o_host, l_host), stream)
     # (b) pipelined, as a caller serving a stream of requests runs it: two sets of device buffers,
     # one stream per direction of the host link (the two directions overlap) and one for compute.
     # Every step still copies its Q, K, V in and its O, LSE out inside the timed region; step i's
@@ -683,33 +740,55 @@ def run_ours(args):
         ev["cmp"][b_].record(s_cmp)
         ev["out"][b_].record(s_out)
 
-    def pipelined(n_steps):
+    def pipelined(n_steps, timed=False):
+        marks = []
         for i in range(n_steps):
             b_ = i & 1
             qd, kd, vd, od, ld, oh, lh = sets[b_]
+            te = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if timed else None
             s_in.wait_event(ev["cmp"][b_])  # step i-2's attention has read this input set
+            if timed:
+                te[0].record(s_in)
             with torch.cuda.stream(s_in):
                 for dst, src in zip((qd, kd, vd), host):
                     dst.copy_(src, non_blocking=True)
+            if timed:
+                te[1].record(s_in)
             ev["in"][b_].record(s_in)
             s_cmp.wait_event(ev["in"][b_])
             s_cmp.wait_event(ev["out"][b_])  # step i-2's copy-out has read this output set
+            if timed:
+                te[2].record(s_cmp)
             usp.usp_attention(qd, kd, vd, B, S, H, D, scale, w.causal, w.ulysses_degree,
                               w.ring_degree, od, ld, ws, nbytes, seq, None, w.order, o_code, s_cmp)
+            if timed:
+                te[3].record(s_cmp)
             ev["cmp"][b_].record(s_cmp)
             s_out.wait_event(ev["cmp"][b_])
+            if timed:
+                te[4].record(s_out)
             with torch.cuda.stream(s_out):
                 oh.copy_(od, non_blocking=True)
                 lh.copy_(ld, non_blocking=True)
+            if timed:
+                te[5].record(s_out)
             ev["out"][b_].record(s_out)
+            if timed:
+                marks.append(te)
+        return marks
 
     pipelined(4)
     torch.cuda.synchronize()
     p_start, p_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     p_start.record(s_in)
-    pipelined(e2e_steps)
+    marks = pipelined(e2e_steps, timed=True)
     p_end.record(s_out)  # after the last copy-out, which depends on every earlier operation
     p_end.synchronize()
+    # per-stage durations inside the pipeline, and the attention's start-to-start period
+    pipe_stages = {"h2d": [m[0].elapsed_time(m[1]) for m in marks],
+                   "attention": [m[2].elapsed_time(m[3]) for m in marks],
+                   "d2h": [m[4].elapsed_time(m[5]) for m in marks],
+                   "attention_period": [a[2].elapsed_time(b_[2]) for a, b_ in zip(marks, marks[1:])]}
     e2e_value, _ = aggregate(e2e_steps * flops, p_start.elapsed_time(p_end) / 1000.0, world, device)
     nvtx.range_pop()
     if usp.usp_check_status(ws, s_cmp) != usp.USP_OK:
@@ -782,7 +861,17 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h,
                 "mode": "pipelined: step i's copy-in overlaps step i-1's attention and copy-out "
                         "(two device buffer sets, one stream per link direction)",
-                "serial_value": e2e_serial / 1e12},
+                "serial_value": e2e_serial / 1e12, "host_link": link,
+                # median ms of each stage (and of the attention's start-to-start period when
+                # pipelined), from events between the stages
+                "serial_stage_ms": {n: statistics.median(x) for n, x in serial_stages.items()},
+                "pipelined_stage_ms": {n: statistics.median(x) for n, x in pipe_stages.items() if x},
+                # the pipelined figure this run's link rates predict: the FLOPs of a step over the
+                # larger of its device time and its copies in both directions at once (a short
+                # burst; back-to-back steps keep the link busier, so the figure can exceed it a
+                # little)
+                "pipelined_estimate": flops / max(t_max * 1000.0 / args.steps,
+                                                  link["both_ms"]) / 1e9},
         "qkvpacked": {"value": packed_value / 1e12, "unit": "TFLOP/s",
                       "ms_per_step": packed_ms / packed_steps, "steps": packed_steps,
                       "input": "bf16 [B][S][3][H][D] through usp_attention_qkvpacked"},
