@@ -32,7 +32,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
                                                         long long lse_stride, long long n_vec,
                                                         int D, void* __restrict__ o_out,
                                                         float* __restrict__ lse_out) {
-  pdl_prologue();
+  pdl_launch_dependents();
+  bool waited = false;  // the first iteration's indices come before the wait
   const int qpv = D >> 2;  // float4 per vector
   const long long total = n_vec * qpv;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -48,6 +49,13 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
       valid[u] = i < total;
       vec[u] = valid[u] ? i / qpv : 0;
       q[u] = static_cast<int>(i - vec[u] * qpv);
+    }
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
 #pragma unroll
       for (int k = 0; k < NP; ++k)
         l[u][k] = valid[u] ? __ldg(lse_parts + k * lse_stride + vec[u]) : -INFINITY;
@@ -117,7 +125,8 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __rest
                                                              float* __restrict__ lse_out,
                                                              const __grid_constant__ MergeMap m) {
   constexpr int kB = NP <= 2 ? 4 : (NP <= 4 ? 2 : 1);  // float4 slots per lane per batch
-  pdl_prologue();
+  pdl_launch_dependents();
+  bool waited = false;  // the first row's placement comes from the parameters before the wait
   const int lane = threadIdx.x & 31;
   const long long total = m.row0[m.n_blocks];
   const long long step = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
@@ -139,6 +148,10 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __rest
     const long long src_vec = m.vec0[lo] + rr * hh;          // W vector of (row, head 0)
     const long long dst_vec = (b * m.S + pos) * m.H + m.hoff[lo];
     const int nf4 = hh * qpv;
+    if (!waited) {  // warp-uniform
+      pdl_wait();
+      waited = true;
+    }
     for (int f0 = 0; f0 < nf4; f0 += 32 * kB) {
       float l_[kB][NP];
       float4 o_[kB][NP];

@@ -114,6 +114,14 @@ __device__ __forceinline__ void pdl_prologue() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// The two halves of pdl_prologue(), for kernels that compute their first addresses from the
+// parameters before waiting: launch_dependents at the start, wait before the first global memory
+// access (load or store).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------------------------
 // tcgen05
 // ---------------------------------------------------------------------------------------------

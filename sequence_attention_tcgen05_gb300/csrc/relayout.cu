@@ -70,12 +70,15 @@ __device__ __forceinline__ RowPlace place_row(const RelayoutParams& p, long long
 constexpr int kNV = 8;  // vectors in flight per lane (4 KB per warp with 16-byte vectors)
 
 // One warp per (tensor, row, head group) block: the lanes issue every vector load of the block
-// (up to kNV per lane per batch) before the first store.
+// (up to kNV per lane per batch) before the first store.  Under programmatic dependent launch a
+// warp places its first block before it waits for the previous kernel of the stream: at 57 MB a
+// launch, that moved the head->seq re-layout of O from 5.34 to 5.78 TB/s back to back.
 template <int VEC>
 __global__ void __launch_bounds__(256) relayout_block_kernel(const __grid_constant__ RelayoutParams p,
                                                              long long n_blocks) {
   using T = typename Vec<VEC>::T;
-  pdl_prologue();
+  pdl_launch_dependents();
+  bool waited = false;  // the first block's addresses come from the parameters before the wait
   const int lane = threadIdx.x & 31;
   const long long rows = p.row0[p.R];
   const long long per_tensor = rows * p.U;
@@ -93,6 +96,10 @@ __global__ void __launch_bounds__(256) relayout_block_kernel(const __grid_consta
     const int nvec = static_cast<int>(hg * p.elem / VEC);
     const T* __restrict__ src = reinterpret_cast<const T*>(p.src[tensor] + (p.dir == 0 ? seq_g : head_elem) * p.elem);
     T* __restrict__ dst = reinterpret_cast<T*>(p.dst[tensor] + (p.dir == 0 ? head_elem : seq_g) * p.elem);
+    if (!waited) {  // warp-uniform
+      pdl_wait();
+      waited = true;
+    }
     for (int v0 = 0; v0 < nvec; v0 += 32 * kNV) {
       T buf[kNV];
 #pragma unroll
