@@ -22,6 +22,15 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// An LSE value of a partial: read by every lane that merges one of its vector's 16-byte slots, so
+// the load keeps L1's default caching; a coherent load (not ld.global.nc), because the kernel may
+// start while the kernel that wrote the partials is still running (see pdl_wait in ptx.cuh).
+__device__ __forceinline__ float ld_lse(const float* p) {
+  float v;
+  asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
 // NP partials, U vectors' worth of float4 slots per thread per iteration: every LSE and partial
 // load of the iteration is issued before the first is used (a partial whose LSE turns out to be
 // -inf was loaded for nothing but is ignored), so U x NP independent 16-byte loads are in flight.
@@ -58,7 +67,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
     for (int u = 0; u < U; ++u) {
 #pragma unroll
       for (int k = 0; k < NP; ++k)
-        l[u][k] = valid[u] ? __ldg(lse_parts + k * lse_stride + vec[u]) : -INFINITY;
+        l[u][k] = valid[u] ? ld_lse(lse_parts + k * lse_stride + vec[u]) : -INFINITY;
     }
     float4 o[U][NP];
 #pragma unroll
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const float* __rest
         q[i] = f - head[i] * qpv;
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
-          l_[i][k] = f < nf4 ? __ldg(lse_parts + k * lse_stride + src_vec + head[i]) : -INFINITY;
+          l_[i][k] = f < nf4 ? ld_lse(lse_parts + k * lse_stride + src_vec + head[i]) : -INFINITY;
           if (ALL_SEEN && f < nf4)  // every slot was written: load it with its LSE, not after
             o_[i][k] = __ldcs(reinterpret_cast<const float4*>(o_parts + k * o_stride +
                                                               (src_vec + head[i]) * D) + q[i]);

@@ -117,6 +117,11 @@ __device__ __forceinline__ void pdl_prologue() {
 // The two halves of pdl_prologue(), for kernels that compute their first addresses from the
 // parameters before waiting: launch_dependents at the start, wait before the first global memory
 // access (load or store).
+// A kernel launched this way reads the previous kernel's outputs with coherent loads only (plain
+// or ld.global.cs), never ld.global.nc (__ldg): a non-coherent load declares its data constant for
+// the whole kernel, which does not hold before the wait returns, and such a load may then be
+// scheduled ahead of the wait.  (Observed: a merge whose LSE loads were ld.global.nc read the
+// previous round's LSE when it followed, back to back, the copy that wrote them.)
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
