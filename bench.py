@@ -21,7 +21,7 @@ loop whose events sit between the phases.  Times come from CUDA events on the la
             step at a time on one stream.  `host_link` = the copies' rates in this run (each
             direction alone and both at once), `pipelined_estimate` = the pipelined figure they
             predict (the host link is shared with other jobs, so it varies from run to run), and
-            `serial_stage_ms` / `pipelined_stage_ms` = each stage's median time.
+            `serial_stage_ms` / `pipelined_stage_ms` = each stage's median and maximum time.
   roofline  the partial-attention phase alone against the measured dense bf16 tensor peak.
   relayout_merge  GB/s of the step's bandwidth-bound phases, plus separately timed standalone
             measurements of the re-layout entry points on the workload's tensors and of the LSE
@@ -40,6 +40,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -57,19 +58,28 @@ NOMINAL_HBM_GBS = 8000.0
 
 # DRAM bytes (read + write) per launch of the attention kernel, dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture of that workload's launch, with the hash of the kernel
-# sources they were taken on; reported as null once the kernel changes.
+# code they were taken on (kernel_hash); reported as null once that code changes.
 ATTN_TRAFFIC = {
     # one full-size launch: dram__bytes_read.sum 3900705024 + dram__bytes_write.sum 574473984
-    "llm_64k_ring8_zigzag": {"bytes": 3900705024 + 574473984, "kernel_hash": "3501e286fc1d280d"},
+    "llm_64k_ring8_zigzag": {"bytes": 3900705024 + 574473984, "kernel_hash": "ca61122c6c07b3d9"},
 }
 L2_BYTES = 129e6
 
 
+def code_of(src: str) -> str:
+    """C/C++ source without its comments and whitespace (the code the compiler sees)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return re.sub(r"\s+", "", src)
+
+
 def kernel_hash() -> str:
+    """Hash of the attention kernel's code (attn.cu and ptx.cuh without comments or whitespace):
+    the recorded DRAM traffic stays attached to the code it was measured on."""
     h = hashlib.sha256()
     for f in ("attn.cu", "ptx.cuh"):
-        with open(os.path.join(ROOT, "sequence_attention_tcgen05_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "sequence_attention_tcgen05_gb300", "csrc", f)) as fh:
+            h.update(code_of(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -862,10 +872,13 @@ def run_ours(args):
                 "mode": "pipelined: step i's copy-in overlaps step i-1's attention and copy-out "
                         "(two device buffer sets, one stream per link direction)",
                 "serial_value": e2e_serial / 1e12, "host_link": link,
-                # median ms of each stage (and of the attention's start-to-start period when
-                # pipelined), from events between the stages
-                "serial_stage_ms": {n: statistics.median(x) for n, x in serial_stages.items()},
-                "pipelined_stage_ms": {n: statistics.median(x) for n, x in pipe_stages.items() if x},
+                # median and maximum ms of each stage (and of the attention's start-to-start
+                # period when pipelined), from events between the stages: a maximum far above the
+                # median is a stall of the shared host link, not of the kernels
+                "serial_stage_ms": {n: {"median": statistics.median(x), "max": max(x)}
+                                    for n, x in serial_stages.items()},
+                "pipelined_stage_ms": {n: {"median": statistics.median(x), "max": max(x)}
+                                       for n, x in pipe_stages.items() if x},
                 # the pipelined figure this run's link rates predict: the FLOPs of a step over the
                 # larger of its device time and its copies in both directions at once (a short
                 # burst; back-to-back steps keep the link busier, so the figure can exceed it a
