@@ -88,6 +88,14 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def roofline_peak(peaks: dict, timed_ms: float):
+    """(bf16 peak, sustained?) for a timed region of `timed_ms` ms of device time: the burst peak
+    for a kernel timed alone, the sustained one (cuBLAS over a seconds-long loop under the power
+    cap) for a kernel timed inside a long run of steps."""
+    sustained = timed_ms >= SUSTAINED_MS
+    return (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]), sustained
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -815,10 +823,7 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
     att_s = phases["attention"] / 1000.0 / breakdown_steps
     achieved = flops / att_s / 1e12
-    # the burst peak for a kernel timed alone, the sustained one (cuBLAS over a seconds-long loop
-    # under the power cap) for a kernel timed inside a long run of steps
-    sustained = total_ms >= SUSTAINED_MS
-    peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    peak, sustained = roofline_peak(peaks, total_ms)
     traffic = ATTN_TRAFFIC.get(w.name)
     traffic_bytes = traffic["bytes"] if traffic and traffic["kernel_hash"] == kernel_hash() else None
     pb = phase_bytes(w, out_elem, ring_mode)

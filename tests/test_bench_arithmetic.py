@@ -67,3 +67,21 @@ def test_causal_zigzag_merge_bytes():
 def test_single_ring_rank_has_no_merge():
     for name in ("flux_1024_u2", "flux_1008_uaa2", "flux_1008_uaa3", "tiny_uaa3"):
         assert bench.phase_bytes(synth.WORKLOADS[name], 2, "none")["merge"] == 0
+
+
+def test_roofline_peak_by_timed_length():
+    """A timed region of at least SUSTAINED_MS of device time divides by the sustained bf16 peak,
+    a shorter one by the burst peak."""
+    peaks = {"bf16_tflops": 1842.5, "bf16_tflops_sustained": 1679.4, "hbm_gbs": 6791.4}
+    assert bench.roofline_peak(peaks, 20 * 21.2) == (1679.4, True)      # 64K ring, 20 steps
+    assert bench.roofline_peak(peaks, 100 * 0.167) == (1842.5, False)   # FLUX, 100 steps
+    assert bench.roofline_peak(peaks, bench.SUSTAINED_MS) == (1679.4, True)
+
+
+def test_kernel_hash_ignores_comments_and_whitespace():
+    """The DRAM traffic recorded for the attention kernel stays valid across comment edits and is
+    dropped when the code changes."""
+    code = "int f(int x) {\n  // one\n  return x + 1; /* two\n lines */\n}\n"
+    assert bench.code_of(code) == "intf(intx){returnx+1;}"
+    assert bench.code_of(code.replace("// one", "// another comment")) == bench.code_of(code)
+    assert bench.code_of(code.replace("x + 1", "x + 2")) != bench.code_of(code)
