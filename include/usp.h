@@ -25,7 +25,12 @@
  *     compiled into the library).  On the host it caches the plans of recent argument sets
  *     (thread-safe); calls on different streams are independent if their buffers are.
  *   - Errors are return codes; usp_last_error() gives a thread-local message for the last
- *     failing call of the calling thread.  On any error nothing has been launched.
+ *     failing call of the calling thread.  Argument and workspace errors are found before
+ *     anything is launched; a CUDA error from a launch leaves the call's earlier launches in the
+ *     stream.
+ *   - Stream order holds for every kernel.  The re-layout and merge kernels use programmatic
+ *     dependent launch: they may be scheduled while the previous kernel of the stream drains,
+ *     but touch no memory before it has completed.
  *   - Head dimension D must be 64 or 128 for attention; re-layout accepts any D >= 1.
  */
 #ifndef USP_GB300_H
