@@ -26,8 +26,9 @@
  *     (thread-safe); calls on different streams are independent if their buffers are.
  *   - Errors are return codes; usp_last_error() gives a thread-local message for the last
  *     failing call of the calling thread.  Argument and workspace errors are found before
- *     anything is launched; a CUDA error from a launch leaves the call's earlier launches in the
- *     stream.
+ *     anything is launched (except that usp_attention_noalloc has cleared its status word when
+ *     a plan exceeds this build's limits); a CUDA error from a launch leaves the call's earlier
+ *     launches in the stream.
  *   - Stream order holds for every kernel.  The re-layout and merge kernels use programmatic
  *     dependent launch: they may be scheduled while the previous kernel of the stream drains,
  *     but touch no memory before it has completed.

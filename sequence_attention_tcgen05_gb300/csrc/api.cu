@@ -854,33 +854,14 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     return fail(USP_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, g.total);
   if (S == 0) return USP_OK;
   if (usp_status_t st = check_device()) return st;
-  if (usp_status_t st = mark(0)) return st;
   char* ws = static_cast<char*>(workspace);
   const int U = g.U, R = g.R;
   usp_status_t st;
 
-  // 1. Q, K, V of virtual rank (r, u): in place in the global tensor when ring chunk r is one affine
-  //    run of rows (the head-sharded view is then pure addressing); otherwise a fused reorder +
-  //    seq -> head re-layout into the workspace first.
-  if (!g.fused_in) {
-    RelayoutParams rp;
-    fill_relayout_grid(rp, g, D, 2);
-    rp.n_tensors = 3;
-    rp.seq_rs = in_rs;
-    rp.src[0] = static_cast<const char*>(q); rp.dst[0] = ws + g.off_q;
-    rp.src[1] = static_cast<const char*>(k); rp.dst[1] = ws + g.off_k;
-    rp.src[2] = static_cast<const char*>(v); rp.dst[2] = ws + g.off_v;
-    rp.dir = 0;
-    if ((st = launch_relayout(rp, stream))) return st;
-    ++n_launch[0];
-  }
-  if ((st = mark(1))) return st;
-
-  // 2. attention over every (Ulysses rank, q ring chunk, ring step) pair in one launch: one
-  //    segment per chunk pair (ring partials or, with one ring rank, the final output), or one
-  //    chain per piece of query rows across all ring steps (fused ring: the final output).
-  //    A thread that repeats its previous call (same plan, buffers and settings) relaunches the
-  //    parameters it built then, without encoding the tensor maps again.
+  // The attention launch's parameters are prepared on the host before anything is launched, so
+  // that a call failing on the host leaves nothing in the stream.  A thread that repeats its
+  // previous call (same plan, buffers and settings) reuses the parameters it built then, without
+  // encoding the tensor maps again.
   struct CallMemo {
     std::shared_ptr<const PlanEntry> pe;
     const void *q, *k, *v, *o, *lse, *ws;
@@ -894,12 +875,9 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
   const unsigned long long budget = wait_budget_ns();
   const int withhold = withhold_loads();
   const bool partials = R > 1 && !g.fused_ring;
-  if (memo.pe == pe && memo.q == q && memo.k == k && memo.v == v && memo.o == o && memo.lse == lse &&
-      memo.ws == workspace && memo.in_rs == in_rs && memo.scale == scale && memo.budget == budget &&
-      memo.withhold == withhold) {
-    if ((st = run_attention(memo.launches, D, stream))) return st;
-    n_launch[1] = static_cast<int>(memo.launches.size());
-  } else {
+  if (!(memo.pe == pe && memo.q == q && memo.k == k && memo.v == v && memo.o == o &&
+        memo.lse == lse && memo.ws == workspace && memo.in_rs == in_rs && memo.scale == scale &&
+        memo.budget == budget && memo.withhold == withhold)) {
     memo.pe.reset();
     static thread_local AttnParams params;
     AttnParams& p = params;
@@ -962,9 +940,31 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     memo.pe = pe;
     memo.q = q; memo.k = k; memo.v = v; memo.o = o; memo.lse = lse; memo.ws = workspace;
     memo.in_rs = in_rs; memo.scale = scale; memo.budget = budget; memo.withhold = withhold;
-    if ((st = run_attention(memo.launches, D, stream))) return st;
-    n_launch[1] = static_cast<int>(memo.launches.size());
   }
+  if ((st = mark(0))) return st;
+
+  // 1. Q, K, V of virtual rank (r, u): in place in the global tensor when ring chunk r is one affine
+  //    run of rows (the head-sharded view is then pure addressing); otherwise a fused reorder +
+  //    seq -> head re-layout into the workspace first.
+  if (!g.fused_in) {
+    RelayoutParams rp;
+    fill_relayout_grid(rp, g, D, 2);
+    rp.n_tensors = 3;
+    rp.seq_rs = in_rs;
+    rp.src[0] = static_cast<const char*>(q); rp.dst[0] = ws + g.off_q;
+    rp.src[1] = static_cast<const char*>(k); rp.dst[1] = ws + g.off_k;
+    rp.src[2] = static_cast<const char*>(v); rp.dst[2] = ws + g.off_v;
+    rp.dir = 0;
+    if ((st = launch_relayout(rp, stream))) return st;
+    ++n_launch[0];
+  }
+  if ((st = mark(1))) return st;
+
+  // 2. attention over every (Ulysses rank, q ring chunk, ring step) pair in one launch: one
+  //    segment per chunk pair (ring partials or, with one ring rank, the final output), or one
+  //    chain per piece of query rows across all ring steps (fused ring: the final output).
+  if ((st = run_attention(memo.launches, D, stream))) return st;
+  n_launch[1] = static_cast<int>(memo.launches.size());
   if ((st = mark(2))) return st;
 
   // 3. merge the ring partials straight into the global layout (the head -> seq all-to-all and the

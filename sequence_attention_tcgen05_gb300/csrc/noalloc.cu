@@ -98,6 +98,12 @@ extern "C" usp_status_t usp_attention_noalloc(const void* q, const void* k, cons
     return usp_attention(q, k, v, B, S, H, D, scale, causal, ulysses_degree, ring_degree, seq_lens,
                          head_counts, order, o, o_dt, lse, nullptr, 0, stream);
   }
+  // the pointer checks usp_attention makes, before the status word is cleared in the stream
+  auto misaligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; };
+  if (!q || !k || !v || !o) return usp::fail(USP_ERR_INVALID_ARG, "NULL q, k, v or o");
+  if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
+      (lse && misaligned(lse, 4)))
+    return usp::fail(USP_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
   if (need > kScratchBytes)
     return usp::fail(USP_ERR_WORKSPACE,
                      "usp_attention_noalloc: this problem needs %zu bytes of scratch, more than the "
