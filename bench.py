@@ -227,17 +227,13 @@ def workload(name: str):
 def phase_bytes(w, out_elem: int, ring_mode: str):
     """Algorithmic HBM bytes of the bandwidth-bound phases (each element read once + written once).
 
-    Q/K/V are re-laid by a separate pass only for zigzag order with several ring ranks whose
-    half-chunks are unequal or not whole 128-row tiles (otherwise the attention's tensor maps
-    address each virtual rank's head-sharded view in place); O and LSE are always written in the
-    global layout by the attention (one ring rank, or fused ring steps) or by the merge (separate
-    ring steps)."""
+    Q/K/V are never re-laid by a pass: the attention's tensor maps address each virtual rank's
+    head-sharded view in place for every ordering.  O and LSE are always written in the global
+    layout by the attention (one ring rank, or fused ring steps) or by the merge (separate ring
+    steps)."""
     elems = w.B * w.S * w.H * w.D
     rows_h = w.B * w.S * w.H
-    half = w.S // (2 * w.ring_degree)
-    qkv_pass = (w.order == "zigzag" and w.ring_degree > 1 and
-                (w.S % (2 * w.ring_degree) != 0 or half % 128 != 0))
-    b = {"qkv_relayout": 2 * 3 * elems * 2 if qkv_pass else 0}
+    b = {"qkv_relayout": 0}
     if ring_mode == "separate":
         # every partial's LSE is read; only partials whose rows saw a key are read in full (a
         # fully masked chunk pair leaves lse = -inf and the merge skips its O)

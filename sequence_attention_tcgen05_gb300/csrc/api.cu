@@ -222,12 +222,20 @@ struct Grid {
   std::vector<Positions> pos;  // per ring group
   std::vector<int> S_r;        // ring chunk lengths
   std::vector<int> h, hoff;    // head groups
-  // Q/K/V of every virtual rank can be addressed in place in the global tensor (each ring chunk is
-  // one affine run of rows, or two equal half-chunks of whole 128-row tiles under zigzag); otherwise
-  // they are first re-laid into the head-sharded workspace copies.
-  bool fused_in = true;
+  // Q/K/V of every virtual rank are addressed in place in the global tensor.  A ring chunk that is
+  // one affine run of rows has a 4-D map over it; a zigzag chunk of two equal half-chunks of
+  // whole 128-row tiles a 5-D map with a piece dimension; any other zigzag chunk a 4-D "span" map
+  // over the global rows from its first half-chunk's start to its second's end, in which its
+  // second half-chunk starts at map row span_off[r] (0: no span map).  Query runs and key ranges
+  // of a span-mapped chunk never cross its half-chunk boundary (the planner cuts them there), so
+  // the rows of other ranks inside the span are never read as its rows.
+  std::vector<int> span_off;
+  bool span(int r) const { return span_off[r] > 0; }
+  int maprow(int r, int l) const {  // map row of ring-local row l of chunk r
+    return span(r) && l >= pos[r].len[0] ? span_off[r] + (l - pos[r].len[0]) : l;
+  }
   // workspace layout (bytes)
-  size_t off_q = 0, off_k = 0, off_v = 0, off_opart = 0, off_lpart = 0, total = 0;
+  size_t off_opart = 0, off_lpart = 0, total = 0;
   int64_t elems = 0;  // B*S*H*D
   int64_t woff(int r, int u, int d) const {  // element offset of block (r, u) in the W layout
     int64_t off = 0;
@@ -289,12 +297,13 @@ usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int causal, int U, 
   }
   g.hoff.assign(U, 0);
   for (int u = 1; u < U; ++u) g.hoff[u] = g.hoff[u - 1] + g.h[u - 1];
-  // Q/K/V are addressed in place unless a zigzag chunk's two half-chunks differ in length or are not
-  // whole 128-row tiles (a tile must not straddle them); then they are re-laid into the workspace.
-  g.fused_in = true;
+  // span maps for the zigzag chunks whose half-chunks differ in length or are not whole 128-row
+  // tiles (a tile of a 5-D map must not straddle them)
+  g.span_off.assign(R, 0);
   for (int r = 0; r < R; ++r) {
     const Positions& ps = g.pos[r];
-    if (two_pieces(ps) && !(ps.len[0] == ps.len[1] && ps.len[0] % kAttnBM == 0)) g.fused_in = false;
+    if (two_pieces(ps) && !(ps.len[0] == ps.len[1] && ps.len[0] % kAttnBM == 0))
+      g.span_off[r] = ps.start[1] - ps.start[0];
   }
   g.elems = int64_t(B) * S * H * D;
   const int64_t rowsH = int64_t(B) * S * H;
@@ -304,11 +313,6 @@ usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int causal, int U, 
     at = static_cast<size_t>(align_up(static_cast<int64_t>(at + bytes), 256));
     return o;
   };
-  if (!g.fused_in) {
-    g.off_q = take(g.elems * 2);
-    g.off_k = take(g.elems * 2);
-    g.off_v = take(g.elems * 2);
-  }
   g.fused_ring = R > 1 && choose_fused_ring(g, o_dt);
   if (R > 1 && !g.fused_ring) {
     g.off_opart = take(size_t(R) * g.elems * 4);
@@ -345,13 +349,54 @@ SegOut set_final_output(AttnSeg& s, const Grid& g, int r, int u, int oel) {
   return {false, int64_t(g.hoff[u]) * g.D * oel, int64_t(g.hoff[u]) * 4};
 }
 
-// A zigzag chunk addressed in place is two maps' worth of pieces: every run must start on a
+// A zigzag chunk read through a 5-D map is two pieces of whole tiles: every run must start on a
 // 128-row tile so that no tile straddles its half-chunks (runs start at 0 or at the second half
 // for these orderings).
 usp_status_t check_run_start(const Grid& g, int r, const Run& run) {
-  if (g.fused_in && two_pieces(g.pos[r]) && run.q0 % kAttnBM != 0)
+  if (two_pieces(g.pos[r]) && !g.span(r) && run.q0 % kAttnBM != 0)
     return fail(USP_ERR_UNSUPPORTED, "zigzag run at row %d does not start on a 128-row tile", run.q0);
   return USP_OK;
+}
+
+// The links of one ring step for a segment of q_len query rows: the visible keys of K/V chunk r2
+// are its ring-local keys [0, kv_len), key c visible to segment-local query i iff c <= i + diag
+// (kNoDiag: no limit).  One link, or two when chunk r2 has a span map: its first half-chunk's
+// keys, and its second's from their own map row with the diagonal shifted by the first half's
+// length.  A link that no query row sees is left out.
+void add_links(const Grid& g, int r2, int u, int kv_len, int diag, int q_len,
+               std::vector<AttnLink>& links) {
+  const int km = map_index(g, r2, u, 1), vm = map_index(g, r2, u, 2);
+  auto seen = [&](int len, int d) { return len > 0 && (d == kNoDiag || (q_len - 1) + d >= 0); };
+  if (!g.span(r2)) {
+    if (seen(kv_len, diag)) links.push_back({km, vm, 0, kv_len, diag});
+    return;
+  }
+  const int len0 = g.pos[r2].len[0];
+  const int n0 = std::min(kv_len, len0), n1 = kv_len - len0;
+  const int d1 = diag == kNoDiag ? kNoDiag : diag - len0;
+  if (seen(n0, diag)) links.push_back({km, vm, 0, n0, diag});
+  if (seen(n1, d1)) links.push_back({km, vm, g.span_off[r2], n1, d1});
+}
+
+// The runs of ring chunk r, cut where a span-mapped chunk's second half-chunk starts.
+std::vector<Run> cut_at_span(const Grid& g, int r, const std::vector<Run>& runs) {
+  if (!g.span(r)) return runs;
+  const int len0 = g.pos[r].len[0];
+  std::vector<Run> out;
+  for (const Run& run : runs) {
+    if (run.q0 < len0 && run.q0 + run.q_len > len0) {
+      Run a = run, b = run;
+      a.q_len = len0 - run.q0;
+      b.q0 = len0;
+      b.q_len = run.q0 + run.q_len - len0;
+      if (b.diag != kNoDiag) b.diag += len0 - run.q0;
+      out.push_back(a);
+      out.push_back(b);
+    } else {
+      out.push_back(run);
+    }
+  }
+  return out;
 }
 
 // One segment per (ring rank r, ring step k, Ulysses rank u, run of query rows), one link each.
@@ -360,16 +405,19 @@ usp_status_t plan_separate(const Grid& g, int oel, AttnPlan& pl) {
   for (int r = 0; r < g.R; ++r) {
     for (int kstep = 0; kstep < g.R; ++kstep) {
       const int r2 = (r - kstep + g.R) % g.R;
-      const std::vector<Run> runs = plan_runs(g.pos[r], g.pos[r2], g.causal);
+      const std::vector<Run> runs = cut_at_span(g, r, plan_runs(g.pos[r], g.pos[r2], g.causal));
       for (const Run& run : runs)
         if (usp_status_t st = check_run_start(g, r, run)) return st;
       for (int u = 0; u < g.U; ++u) {
         for (const Run& run : runs) {
           AttnSeg s{};
           s.q_map = map_index(g, r, u, 0);
-          s.q_row0 = run.q0; s.q_len = run.q_len;
-          s.link0 = static_cast<int>(pl.links.size()); s.n_links = 1;
-          pl.links.push_back({map_index(g, r2, u, 1), map_index(g, r2, u, 2), 0, run.kv_len, run.diag});
+          s.q_row0 = g.maprow(r, run.q0); s.q_len = run.q_len;
+          // every (ring step, run) segment writes its partial slot, with no link at all if no
+          // row sees a key (o = 0, lse = -inf)
+          s.link0 = static_cast<int>(pl.links.size());
+          add_links(g, r2, u, run.kv_len, run.diag, run.q_len, pl.links);
+          s.n_links = static_cast<int>(pl.links.size()) - s.link0;
           s.n_heads = g.h[u];
           s.grp = u;
           s.o_row0 = run.q0;
@@ -400,6 +448,7 @@ usp_status_t plan_fused(const Grid& g, int oel, AttnPlan& pl) {
     if (Sr == 0) continue;
     std::vector<std::vector<Run>> runs(g.R);
     std::vector<int> cuts = {0, Sr};
+    if (g.span(r)) cuts.push_back(g.pos[r].len[0]);  // pieces never cross the half-chunks
     for (int kstep = 0; kstep < g.R; ++kstep) {
       runs[kstep] = plan_runs(g.pos[r], g.pos[(r - kstep + g.R) % g.R], g.causal);
       for (const Run& run : runs[kstep]) {
@@ -414,17 +463,16 @@ usp_status_t plan_fused(const Grid& g, int oel, AttnPlan& pl) {
       for (int u = 0; u < g.U; ++u) {
         AttnSeg s{};
         s.q_map = map_index(g, r, u, 0);
-        s.q_row0 = a; s.q_len = b - a;
+        s.q_row0 = g.maprow(r, a); s.q_len = b - a;
         s.link0 = static_cast<int>(pl.links.size());
         for (int kstep = 0; kstep < g.R; ++kstep) {
           const int r2 = (r - kstep + g.R) % g.R;
           const Run* run = nullptr;
           for (const Run& x : runs[kstep])
             if (x.q0 <= a && a < x.q0 + x.q_len) run = &x;
-          if (!run || run->kv_len == 0) continue;
+          if (!run) continue;
           const int diag = run->diag == kNoDiag ? kNoDiag : run->diag + (a - run->q0);
-          if (diag != kNoDiag && (b - a - 1) + diag < 0) continue;  // no row of the piece sees a key
-          pl.links.push_back({map_index(g, r2, u, 1), map_index(g, r2, u, 2), 0, run->kv_len, diag});
+          add_links(g, r2, u, run->kv_len, diag, b - a, pl.links);  // none if no row sees a key
         }
         s.n_links = static_cast<int>(pl.links.size()) - s.link0;
         s.n_heads = g.h[u];
@@ -499,8 +547,8 @@ bool choose_fused_ring(const Grid& g, usp_dtype_t o_dt) {
   // merge bytes: every partial LSE, the O of partials whose rows saw a key, the final O and LSE
   double seen_vec = 0;
   for (const AttnSeg& s : sep.segs) {
+    if (s.n_links == 0) continue;  // no row sees a key (a later link never sees more rows)
     const AttnLink& lk = sep.links[s.link0];
-    if (lk.kv_len == 0) continue;
     const int rows = lk.diag == kNoDiag ? s.q_len : std::max(0, s.q_len - std::max(0, -lk.diag));
     seen_vec += double(rows) * s.n_heads * g.B;
   }
@@ -884,31 +932,23 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     std::memset(&p, 0, sizeof(p));
     for (int r = 0; r < R; ++r) {
       for (int u = 0; u < U; ++u) {
-        const void* base[3];
-        int64_t row_stride, batch_stride;
+        // virtual rank (r, u)'s head-sharded view, in place: the chunk's rows from its first,
+        // heads [hoff_u, hoff_u + h_u)
         int64_t piece_rows = std::max(1, g.S_r[r]), piece_stride = 0;
         int n_pieces = 1;
-        if (g.fused_in) {
-          const int64_t e0 = int64_t(g.pos[r].start[0]) * in_rs + int64_t(g.hoff[u]) * D;
-          base[0] = static_cast<const uint16_t*>(q) + e0;
-          base[1] = static_cast<const uint16_t*>(k) + e0;
-          base[2] = static_cast<const uint16_t*>(v) + e0;
-          row_stride = int64_t(g.pos[r].stride) * in_rs;
-          batch_stride = int64_t(S) * in_rs;
-          if (two_pieces(g.pos[r])) {  // zigzag chunk: its two half-chunks
-            piece_rows = g.pos[r].len[0];
-            n_pieces = 2;
-            piece_stride = int64_t(g.pos[r].start[1] - g.pos[r].start[0]) * in_rs;
-          }
-        } else {
-          const int64_t off = g.woff(r, u, D) * 2;
-          base[0] = ws + g.off_q + off;
-          base[1] = ws + g.off_k + off;
-          base[2] = ws + g.off_v + off;
-          row_stride = int64_t(g.h[u]) * D;
-          batch_stride = int64_t(g.S_r[r]) * row_stride;
+        const int64_t e0 = int64_t(g.pos[r].start[0]) * in_rs + int64_t(g.hoff[u]) * D;
+        const void* base[3] = {static_cast<const uint16_t*>(q) + e0, static_cast<const uint16_t*>(k) + e0,
+                               static_cast<const uint16_t*>(v) + e0};
+        const int64_t row_stride = int64_t(g.pos[r].stride) * in_rs;
+        int64_t batch_stride = int64_t(S) * in_rs;
+        if (g.span(r)) {  // zigzag chunk with ragged half-chunks: the span of global rows over both
+          piece_rows = g.span_off[r] + g.pos[r].len[1];
+        } else if (two_pieces(g.pos[r])) {  // zigzag chunk: its two half-chunks as two pieces
+          piece_rows = g.pos[r].len[0];
+          n_pieces = 2;
+          piece_stride = int64_t(g.pos[r].start[1] - g.pos[r].start[0]) * in_rs;
         }
-        if (B == 1) batch_stride = std::max<int64_t>(1, g.S_r[r]) * row_stride;
+        if (B == 1) batch_stride = piece_rows * n_pieces * row_stride;
         for (int t = 0; t < 3; ++t) {
           const int mi = map_index(g, r, u, t);
           if ((st = make_qkv_map(&p.maps[mi], base[t], g.h[u], D, piece_rows, n_pieces, B, row_stride,
@@ -943,21 +983,8 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
   }
   if ((st = mark(0))) return st;
 
-  // 1. Q, K, V of virtual rank (r, u): in place in the global tensor when ring chunk r is one affine
-  //    run of rows (the head-sharded view is then pure addressing); otherwise a fused reorder +
-  //    seq -> head re-layout into the workspace first.
-  if (!g.fused_in) {
-    RelayoutParams rp;
-    fill_relayout_grid(rp, g, D, 2);
-    rp.n_tensors = 3;
-    rp.seq_rs = in_rs;
-    rp.src[0] = static_cast<const char*>(q); rp.dst[0] = ws + g.off_q;
-    rp.src[1] = static_cast<const char*>(k); rp.dst[1] = ws + g.off_k;
-    rp.src[2] = static_cast<const char*>(v); rp.dst[2] = ws + g.off_v;
-    rp.dir = 0;
-    if ((st = launch_relayout(rp, stream))) return st;
-    ++n_launch[0];
-  }
+  // 1. Q, K, V of virtual rank (r, u) are read in place (the first all-to-all and the reorder are
+  //    the tensor maps' addressing): no pass.
   if ((st = mark(1))) return st;
 
   // 2. attention over every (Ulysses rank, q ring chunk, ring step) pair in one launch: one
@@ -1098,18 +1125,23 @@ int usp_plan_chains(int S, int ulysses_degree, int ring_degree, int causal, usp_
     return -1;
   AttnPlan pl;
   if (plan_fused(g, 4, pl) != USP_OK) return -1;
+  // one record per (piece, ring step): the two links of a span-mapped K/V chunk (its half-chunks)
+  // are reported as the one key range [0, kv_len) of the chunk they split
   int n = 0;
   for (const AttnSeg& s : pl.segs) {
     const int r = s.q_map / (3 * g.U), u = s.grp;
-    for (int i = 0; i < s.n_links; ++i) {
+    for (int i = 0; i < s.n_links;) {
       const AttnLink& lk = pl.links[s.link0 + i];
       const int r2 = lk.k_map / (3 * g.U);
+      int kv_len = lk.kv_len, j = i + 1;
+      for (; j < s.n_links && pl.links[s.link0 + j].k_map == lk.k_map; ++j) kv_len += pl.links[s.link0 + j].kv_len;
       if (out && n < cap) {
         int32_t* rec = out + 8 * n;
-        rec[0] = u; rec[1] = r; rec[2] = s.q_row0; rec[3] = s.q_len;
-        rec[4] = (r - r2 + g.R) % g.R; rec[5] = r2; rec[6] = lk.kv_len; rec[7] = lk.diag;
+        rec[0] = u; rec[1] = r; rec[2] = s.o_row0; rec[3] = s.q_len;
+        rec[4] = (r - r2 + g.R) % g.R; rec[5] = r2; rec[6] = kv_len; rec[7] = lk.diag;
       }
       ++n;
+      i = j;
     }
   }
   return n;

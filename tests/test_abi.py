@@ -115,21 +115,20 @@ def test_workspace_size(L, monkeypatch):
     monkeypatch.setenv("USP_RING_MERGE", "separate")
     r = usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3)
     assert 3 * 1000 * 4 * 64 * 4 + 3 * 1000 * 4 * 4 <= r <= 3 * 1000 * 4 * 64 * 4 + 3 * 1000 * 4 * 4 + 1024
-    # zigzag ring: additionally the head-sharded bf16 copies of Q, K, V
-    z = usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3, "zigzag")
-    assert z >= r + 3 * 1000 * 4 * 64 * 2
-    # zigzag with equal half-chunks of whole 128-row tiles (64K tokens, ring 8: 16 x 4096) is
-    # addressed in place: the same size as contiguous order, no copies
+    # every ordering is addressed in place: zigzag needs no copies of Q, K, V, whether its
+    # half-chunks are whole 128-row tiles (64K tokens, ring 8: 16 x 4096: a piece dimension) or
+    # not (1000 tokens over 6 half-chunks; 65535 tokens: a span map per chunk)
+    assert usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3, "zigzag") == r
     zc = usp.usp_attention_workspace_size(1, 65536, 32, 128, 1, 8, "contiguous")
-    zz = usp.usp_attention_workspace_size(1, 65536, 32, 128, 1, 8, "zigzag")
-    assert zz == zc > 8 * 65536 * 32 * 128 * 4
-    # half-chunks of 4095.5 rows on average (65535 tokens) are not whole tiles: copies again
-    assert usp.usp_attention_workspace_size(1, 65535, 32, 128, 1, 8, "zigzag") > zc
+    assert usp.usp_attention_workspace_size(1, 65536, 32, 128, 1, 8, "zigzag") == zc > 8 * 65536 * 32 * 128 * 4
+    assert (usp.usp_attention_workspace_size(1, 65535, 32, 128, 1, 8, "zigzag") ==
+            usp.usp_attention_workspace_size(1, 65535, 32, 128, 1, 8, "contiguous"))
     # fused ring steps write the final output directly: no partial slots
     monkeypatch.setenv("USP_RING_MERGE", "fused")
     assert usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3) == 256
     assert usp.usp_attention_workspace_size(1, 65536, 32, 128, 1, 8, "zigzag", causal=True) == 256
-    assert usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3, "zigzag") == z - (r - 256)
+    assert usp.usp_attention_workspace_size(1, 65535, 32, 128, 1, 8, "zigzag", causal=True) == 256
+    assert usp.usp_attention_workspace_size(1, 1000, 4, 64, 1, 3, "zigzag") == 256
     assert usp.usp_attention_workspace_size(1, 10, 4, 96, 1, 1) == 0
     assert usp.usp_attention_workspace_size(1, 10, 4, 64, 5, 4) == 0
 

@@ -56,13 +56,17 @@ def test_noalloc_matches_oracle_three_calls(monkeypatch):
     _call_and_check(t, 2, 600, 3, 128, 1, 4, True, "zigzag", t.float32, seed=3)
 
 
-def test_noalloc_rejects_problems_beyond_the_scratch():
-    """A 64K-token zigzag ring of 8 whose half-chunks are not whole 128-row tiles (65535 tokens)
-    needs head-sharded copies of Q, K and V (1.6 GB): rejected before any launch."""
+def test_noalloc_rejects_problems_beyond_the_scratch(monkeypatch):
+    """A 64K-token causal zigzag ring of 8 run with separate ring steps needs 8 fp32 partial
+    slots of O (8.6 GB): rejected before any launch.  With the ring steps fused it needs only the
+    status word, also when its half-chunks are not whole 128-row tiles (65535 tokens)."""
     build.build_library()
     L = usp.lib()
+    monkeypatch.setenv("USP_RING_MERGE", "separate")
     st = L.usp_attention_noalloc(256, 256, 256, 1, 65535, 32, 128, 0.08, 1, 1, 8, None, None, 1,
                                  256, usp.USP_FP32, 256, None, None)
     assert st == usp.USP_ERR_WORKSPACE
     msg = L.usp_last_error().decode()
     assert "128 MiB" in msg and "needs" in msg
+    monkeypatch.setenv("USP_RING_MERGE", "fused")
+    assert usp.usp_attention_workspace_size(1, 65535, 32, 128, 1, 8, "zigzag", causal=True) == 256
