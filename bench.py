@@ -1,9 +1,11 @@
 #!/usr/bin/env python
 """Benchmark of usp_attention, the whole context-parallel attention path, on synthetic inputs.
 
-One step = one usp_attention call on the workload (fused reorder + seq->head re-layout of Q, K, V;
-the partial-attention launch over every chunk pair; the LSE merge of ring partials; the fused
-head->seq re-layout of O and LSE).  Inputs are resident in HBM when the timed region starts; the
+One step = one usp_attention call on the workload: Q, K, V read in place through each virtual
+rank's tensor maps (the reorder and the seq->head all-to-all are addressing), the attention launch
+over every chunk pair or ring chain, the LSE merge of ring partials when the ring steps run
+separately, and O and LSE written in the global layout (the head->seq all-to-all as store
+addressing).  Inputs are resident in HBM when the timed region starts; the
 L2 cache is flushed between steps (outside the step's events) because the inputs of the default
 workload fit in L2.  The flush READS a 256 MiB buffer: a flush that writes would leave up to the
 whole L2 dirty, and writing those lines back would then be charged to the timed kernels.  Each

@@ -190,11 +190,13 @@ usp_status_t usp_lse_merge(int n_parts, const float* o_parts, int64_t o_part_str
  *   workspace: device scratch of at least usp_attention_workspace_size(...) bytes, 256-byte
  *   aligned.  Its first 4 bytes are the status word usp_check_status reads and clears; zero
  *   them once before the first call (e.g. allocate the workspace zeroed).
- *   Steps (one stream): (1) the seq->head re-layout of Q, K, V: each virtual rank's head-sharded
- *   view is addressed in place by the attention's tensor maps when its ring chunk is one affine
- *   run of global rows (contiguous or stripe order, one ring rank) or, under zigzag, two equal
- *   half-chunks of whole 128-row tiles (S divisible by 256 * ring_degree); otherwise a fused
- *   reorder + seq->head pass copies Q, K, V into the workspace first.
+ *   Steps (one stream): (1) the seq->head re-layout of Q, K, V (with the ring ordering) is
+ *   addressing, not a pass: each virtual rank's head-sharded view is read in place by the
+ *   attention's tensor maps, one map over its ring chunk when that is one affine run of global
+ *   rows (contiguous or stripe order, one ring rank), a map with a piece dimension over a zigzag
+ *   chunk's two equal half-chunks of whole 128-row tiles (S divisible by 256 * ring_degree), and
+ *   otherwise a map over the global rows spanning both half-chunks, of which only the chunk's
+ *   own rows are read as keys and written as outputs.
  *   (2) One attention launch over every (ring step, chunk pair, head, query block), with fully
  *   masked causal tiles skipped.  With several ring ranks the ring steps are either
  *     - fused: each 256-row query block carries one online softmax across the visible K/V chunks
@@ -238,7 +240,8 @@ usp_status_t usp_attention_qkvpacked(const void* qkv, int B, int S, int H, int D
  *   re-layout.  A skipped phase records its event at the same point as the previous one.
  *   `events` must hold 5 handles (entries may be NULL to skip a record).  If `launches` is not
  *   NULL it receives 4 counts: kernels launched for the Q/K/V re-layout, the attention, the merge
- *   and the output re-layout (0 for a phase that did not run).  Errors as usp_attention. */
+ *   and the output re-layout (0 for a phase that did not run; both re-layouts are addressing in
+ *   this library, so their counts are 0).  Errors as usp_attention. */
 usp_status_t usp_attention_events(const void* q, const void* k, const void* v, int B, int S, int H,
                                   int D, float scale, int causal, int ulysses_degree,
                                   int ring_degree, const int32_t* seq_lens,
@@ -276,8 +279,8 @@ usp_status_t usp_attention_noalloc(const void* q, const void* k, const void* v, 
                                    usp_stream_t stream);
 
 /* Bytes of workspace usp_attention needs for these arguments (0 on invalid arguments): a 256-byte
- * status word, plus Q, K, V copies when they cannot be addressed in place, plus ring_degree fp32
- * partial slots of O and LSE when the ring steps run separately (see usp_attention). */
+ * status word, plus ring_degree fp32 partial slots of O and LSE when the ring steps run
+ * separately (see usp_attention). */
 size_t usp_attention_workspace_size(int B, int S, int H, int D, int causal, int ulysses_degree,
                                     int ring_degree, usp_order_t order, usp_dtype_t o_dt);
 

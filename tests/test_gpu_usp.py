@@ -177,8 +177,8 @@ def _sampled_rows(w, n=512, seed=0):
 @pytest.mark.parametrize("name", ["llm_64k257_ring8_zigzag", "llm_32k_ring4_stripe"])
 def test_anything_large_uneven_causal(name, mode, monkeypatch):
     """Ring Anything at large, uneven causal sizes: 65793 tokens over a zigzag ring of 8 (half-
-    chunks of 4111/4112 rows: the fused reorder + seq->head copy path) and 32771 tokens over a
-    stripe ring of 4; sampled rows of two heads against the oracle."""
+    chunks of 4111/4112 rows, read through span maps) and 32771 tokens over a stripe ring of 4;
+    sampled rows (every half-chunk boundary among them) of two heads against the oracle."""
     set_ring_mode(monkeypatch, mode)
     w = synth.WORKLOADS[name]
     _check_heads(w, [0, w.H - 1], _sampled_rows(w))
@@ -193,13 +193,13 @@ def test_ulysses_anything_24_heads_over_5():
 
 @pytest.mark.parametrize("U,R,order,causal,mode", [
     (1, 1, "contiguous", False, "none"), (2, 1, "contiguous", True, "none"),
-    (1, 3, "zigzag", True, "fused"), (1, 3, "zigzag", True, "separate"),   # zigzag copy path
+    (1, 3, "zigzag", True, "fused"), (1, 3, "zigzag", True, "separate"),   # ragged: span maps
     (2, 2, "stripe", True, "fused"), (1, 2, "zigzag", True, "separate"),
     (3, 2, "contiguous", False, "fused"),
 ])
 def test_qkvpacked_matches_oracle(U, R, order, causal, mode, monkeypatch):
     """usp_attention_qkvpacked on a [B][S][3][H][D] input: the tensor maps read the packed rows in
-    place (3*H*D row stride), and the zigzag copy path reads them directly."""
+    place (3*H*D row stride), for zigzag chunks of whole-tile and of ragged half-chunks alike."""
     set_ring_mode(monkeypatch, mode)
     t = torch()
     B, S, H, D = (2, 1000, 4, 128) if order != "zigzag" or R != 2 else (1, 1024, 3, 128)
