@@ -234,8 +234,16 @@ struct Grid {
   int maprow(int r, int l) const {  // map row of ring-local row l of chunk r
     return span(r) && l >= pos[r].len[0] ? span_off[r] + (l - pos[r].len[0]) : l;
   }
+  // Split of a fused ring (non-causal only): query rows [split_row, S_r) of ring chunk split_r in
+  // Ulysses group split_u run as separate ring steps, writing fp32 partials into slots of their
+  // own ([R][B][split_rows][h][D]) that a merge pass combines after the attention.  Their units
+  // form a unit group of their own, dealt after every chain, so that these shorter units fill
+  // the last round of equal-length chains.  split_r = -1: no split.
+  int split_r = -1, split_u = 0, split_row = 0;
+  int split_rows() const { return split_r < 0 ? 0 : S_r[split_r] - split_row; }
+  int64_t split_vec() const { return split_r < 0 ? 0 : int64_t(B) * split_rows() * h[split_u]; }
   // workspace layout (bytes)
-  size_t off_opart = 0, off_lpart = 0, total = 0;
+  size_t off_opart = 0, off_lpart = 0, off_spart = 0, off_slpart = 0, total = 0;
   int64_t elems = 0;  // B*S*H*D
   int64_t woff(int r, int u, int d) const {  // element offset of block (r, u) in the W layout
     int64_t off = 0;
@@ -254,6 +262,17 @@ int ring_env() {
   if (env && std::strcmp(env, "separate") == 0) return 2;
   return 0;
 }
+
+// USP_RING_SPLIT (environment, read at each call): "0" = never split a fused ring, a positive
+// number k = split the last k 256-row blocks of the last ring chunk of the last Ulysses group
+// (non-causal fused rings; for tests), unset = the model decides.
+int split_env() {
+  const char* env = std::getenv("USP_RING_SPLIT");
+  if (!env || !*env) return -1;
+  return std::max(0, std::atoi(env));
+}
+
+void choose_split(Grid& g, usp_dtype_t o_dt);
 
 usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int causal, int U, int R,
                         usp_order_t order, const int32_t* seq_lens, const int32_t* head_counts,
@@ -317,6 +336,11 @@ usp_status_t build_grid(Grid& g, int B, int S, int H, int D, int causal, int U, 
   if (R > 1 && !g.fused_ring) {
     g.off_opart = take(size_t(R) * g.elems * 4);
     g.off_lpart = take(size_t(R) * rowsH * 4);
+  }
+  if (g.fused_ring && !g.causal && S > 0) choose_split(g, o_dt);
+  if (g.split_r >= 0) {
+    g.off_spart = take(size_t(R) * g.split_vec() * D * 4);
+    g.off_slpart = take(size_t(R) * g.split_vec() * 4);
   }
   g.total = at;
   return USP_OK;
@@ -449,6 +473,7 @@ usp_status_t plan_fused(const Grid& g, int oel, AttnPlan& pl) {
     std::vector<std::vector<Run>> runs(g.R);
     std::vector<int> cuts = {0, Sr};
     if (g.span(r)) cuts.push_back(g.pos[r].len[0]);  // pieces never cross the half-chunks
+    if (r == g.split_r && g.split_row > 0) cuts.push_back(g.split_row);
     for (int kstep = 0; kstep < g.R; ++kstep) {
       runs[kstep] = plan_runs(g.pos[r], g.pos[(r - kstep + g.R) % g.R], g.causal);
       for (const Run& run : runs[kstep]) {
@@ -461,6 +486,30 @@ usp_status_t plan_fused(const Grid& g, int oel, AttnPlan& pl) {
     for (size_t ci = 0; ci + 1 < cuts.size(); ++ci) {
       const int a = cuts[ci], b = cuts[ci + 1];
       for (int u = 0; u < g.U; ++u) {
+        if (r == g.split_r && u == g.split_u && a >= g.split_row) {
+          // split rows: one segment per ring step, each writing its fp32 partial slot
+          const int64_t slot_o = g.split_vec() * g.D * 4, slot_l = g.split_vec() * 4;
+          for (int kstep = 0; kstep < g.R; ++kstep) {
+            const int r2 = (r - kstep + g.R) % g.R;
+            AttnSeg s{};
+            s.q_map = map_index(g, r, u, 0);
+            s.q_row0 = g.maprow(r, a); s.q_len = b - a;
+            s.link0 = static_cast<int>(pl.links.size());
+            for (const Run& x : runs[kstep])
+              if (x.q0 <= a && a < x.q0 + x.q_len)
+                add_links(g, r2, u, x.kv_len, x.diag == kNoDiag ? kNoDiag : x.diag + (a - x.q0), b - a,
+                          pl.links);
+            s.n_links = static_cast<int>(pl.links.size()) - s.link0;
+            s.n_heads = g.h[u];
+            s.grp = g.U;  // dealt after every chain
+            s.rev = g.causal;
+            s.o_row0 = a - g.split_row; s.o_bstride = g.split_rows(); s.o_heads = g.h[u];
+            s.o_start0 = 0; s.o_len0 = INT_MAX; s.o_start1 = 0; s.o_stride = 1;
+            pl.outs.push_back({true, int64_t(g.off_spart) + kstep * slot_o, int64_t(g.off_slpart) + kstep * slot_l});
+            pl.segs.push_back(s);
+          }
+          continue;
+        }
         AttnSeg s{};
         s.q_map = map_index(g, r, u, 0);
         s.q_row0 = g.maprow(r, a); s.q_len = b - a;
@@ -558,6 +607,56 @@ bool choose_fused_ring(const Grid& g, usp_dtype_t o_dt) {
   return t_fus <= t_sep + merge_bytes / kPeriodBytes;
 }
 
+// Split of a fused non-causal ring (see Grid): the chains of a ring are all equally long there,
+// and when their count is not a multiple of the SMs the last round runs part-empty.  Running the
+// last k 256-row blocks of one ring chunk as separate ring steps turns those units into R
+// shorter ones dealt after every chain; they fill the last round, at the price of their fp32
+// partials and a merge pass over their rows.  The model deals the units as the kernel does
+// (launch_periods) for every ring chunk of the last Ulysses group and every k, adds the merge's
+// bytes at ~6 TB/s and a launch, and keeps the best split if it saves more than 1 %.
+// USP_RING_SPLIT overrides it.
+void choose_split(Grid& g, usp_dtype_t o_dt) {
+  g.split_r = -1;
+  const int env = split_env();
+  if (env == 0) return;
+  const int u = g.U - 1;
+  auto set = [&](int r, int k) {
+    const int nblk = (g.S_r[r] + kAttnUnitRows - 1) / kAttnUnitRows;
+    k = std::min(k, nblk);
+    g.split_r = r; g.split_u = u; g.split_row = (nblk - k) * kAttnUnitRows;
+  };
+  if (env > 0) {
+    set(g.R - 1, env);
+    return;
+  }
+  constexpr int kModelCtas = 152;
+  constexpr double kPeriodBytes = 6.0e12 * 1.55e-6;  // merge bytes per key-tile period
+  const int oel = o_dt == USP_BF16 ? 2 : 4;
+  auto model = [&]() -> double {
+    AttnPlan pl;
+    if (plan_fused(g, oel, pl) != USP_OK) return 1e30;
+    double t = launch_periods(pl.segs, pl.links, g.B, 2.0, kModelCtas);
+    if (g.split_r >= 0) {
+      const double vec = double(g.split_vec());
+      t += (g.R * vec * (g.D * 4 + 4) + vec * (g.D * oel + 4)) / kPeriodBytes + 2.0;
+    }
+    return t;
+  };
+  const double t0 = model();
+  double best = t0;
+  int best_r = -1, best_k = 0;
+  for (int r = 0; r < g.R; ++r) {
+    const int nblk = (g.S_r[r] + kAttnUnitRows - 1) / kAttnUnitRows;
+    for (int k = 1; k <= nblk; ++k) {
+      set(r, k);
+      const double t = model();
+      if (t < best) { best = t; best_r = r; best_k = k; }
+    }
+  }
+  g.split_r = -1;
+  if (best_r >= 0 && best < 0.99 * t0) set(best_r, best_k);
+}
+
 // ------------------------------------------------------------------------------------------------
 // Plan cache.  Planning a long ring (the chunk-pair runs of every ring step, the ring-mode time
 // model) takes milliseconds on the host; a caller running the same shapes step after step gets
@@ -566,11 +665,12 @@ bool choose_fused_ring(const Grid& g, usp_dtype_t o_dt) {
 // plans are kept.
 // ------------------------------------------------------------------------------------------------
 struct PlanKey {
-  int B, S, H, D, causal, U, R, order, o_dt, ring_env;
+  int B, S, H, D, causal, U, R, order, o_dt, ring_env, split_env;
   std::vector<int32_t> seq_lens, head_counts;
   bool operator==(const PlanKey& o) const {
     return B == o.B && S == o.S && H == o.H && D == o.D && causal == o.causal && U == o.U &&
            R == o.R && order == o.order && o_dt == o.o_dt && ring_env == o.ring_env &&
+           split_env == o.split_env &&
            seq_lens == o.seq_lens && head_counts == o.head_counts;
   }
 };
@@ -589,7 +689,8 @@ std::vector<std::shared_ptr<const PlanEntry>> g_plan_cache;  // most recent firs
 usp_status_t get_plan(int B, int S, int H, int D, int causal, int U, int R, usp_order_t order,
                       const int32_t* seq_lens, const int32_t* head_counts, usp_dtype_t o_dt,
                       std::shared_ptr<const PlanEntry>& out) {
-  PlanKey key{B, S, H, D, causal != 0, U, R, static_cast<int>(order), static_cast<int>(o_dt), ring_env(), {}, {}};
+  PlanKey key{B, S, H, D, causal != 0, U, R, static_cast<int>(order), static_cast<int>(o_dt), ring_env(),
+              split_env(), {}, {}};
   if (seq_lens && U >= 1 && R >= 1 && U <= 16 && R <= 16) key.seq_lens.assign(seq_lens, seq_lens + U * R);
   if (head_counts && U >= 1 && U <= 16) key.head_counts.assign(head_counts, head_counts + U);
   {
@@ -807,7 +908,6 @@ usp_status_t usp_attn_partial(const void* q, const void* k, const void* v, int B
   if ((st = make_qkv_map(&p.maps[2], v, H, D, Sk, 1, B, kv_row_stride, 0, int64_t(Sk) * kv_row_stride))) return st;
 
   p.B = B;
-  p.o_bf16 = o_dt == USP_BF16;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.budget_ns = wait_budget_ns();
@@ -831,6 +931,7 @@ usp_status_t usp_attn_partial(const void* q, const void* k, const void* v, int B
   for (const Run& r : plan_runs(qp, kp, q_pos != nullptr)) {
     AttnSeg s{};
     s.o = o; s.lse = lse;
+    s.o_bf16 = o_dt == USP_BF16;
     s.q_map = 0;
     s.q_row0 = r.q0; s.q_len = r.q_len;
     s.link0 = static_cast<int>(links.size()); s.n_links = 1;
@@ -963,11 +1064,11 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     p.status = reinterpret_cast<uint32_t*>(ws);
     p.budget_ns = budget;
     p.withhold_loads = withhold;
-    p.o_bf16 = partials ? 0 : (o_dt == USP_BF16);
     // the cached plan's segments, bound to this call's output and workspace
     std::vector<AttnSeg> segs = pe->plan.segs;
     for (size_t i = 0; i < segs.size(); ++i) {
       const SegOut& so = pe->plan.outs[i];
+      segs[i].o_bf16 = !so.partial && o_dt == USP_BF16;
       if (so.partial) {
         segs[i].o = ws + so.o_off;
         segs[i].lse = reinterpret_cast<float*>(ws + so.lse_off);
@@ -1022,6 +1123,40 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     if ((st = launch_lse_merge(R, reinterpret_cast<const float*>(ws + g.off_opart), g.elems,
                                reinterpret_cast<const float*>(ws + g.off_lpart), int64_t(B) * S * H,
                                int64_t(B) * S * H, D, o, o_dt == USP_BF16, lse, &mm, stream)))
+      return st;
+    ++n_launch[2];
+  }
+  // 3'. a split fused ring: merge the split rows' partials into the global layout (the rows
+  //    [split_row, S_r) of ring chunk split_r, heads of Ulysses group split_u)
+  if (g.split_r >= 0) {
+    const Positions& ps = g.pos[g.split_r];
+    const int c = g.split_row;
+    MergeMap mm;
+    std::memset(&mm, 0, sizeof(mm));
+    mm.n_blocks = 1;
+    mm.H = H;
+    mm.S = S;
+    mm.vec0[0] = 0;
+    mm.vec0[1] = g.split_vec();
+    mm.row0[0] = 0;
+    mm.row0[1] = int64_t(B) * g.split_rows();
+    mm.S_r[0] = std::max(1, g.split_rows());
+    mm.h[0] = g.h[g.split_u];
+    mm.hoff[0] = g.hoff[g.split_u];
+    if (ps.n_seg > 1 && c >= ps.len[0]) {  // the split rows lie in the second piece
+      mm.p_start0[0] = ps.start[1] + (c - ps.len[0]) * ps.stride;
+      mm.p_len0[0] = INT_MAX;
+    } else {
+      mm.p_start0[0] = ps.start[0] + c * ps.stride;
+      mm.p_len0[0] = ps.n_seg > 1 ? ps.len[0] - c : INT_MAX;
+      mm.p_start1[0] = ps.start[1];
+    }
+    mm.p_stride[0] = ps.stride;
+    mm.all_seen = causal ? 0 : 1;
+    const int64_t vec = g.split_vec();
+    if ((st = launch_lse_merge(R, reinterpret_cast<const float*>(ws + g.off_spart), vec * D,
+                               reinterpret_cast<const float*>(ws + g.off_slpart), vec, vec, D, o,
+                               o_dt == USP_BF16, lse, &mm, stream)))
       return st;
     ++n_launch[2];
   }
@@ -1129,7 +1264,7 @@ int usp_plan_chains(int S, int ulysses_degree, int ring_degree, int causal, usp_
   // are reported as the one key range [0, kv_len) of the chunk they split
   int n = 0;
   for (const AttnSeg& s : pl.segs) {
-    const int r = s.q_map / (3 * g.U), u = s.grp;
+    const int r = s.q_map / (3 * g.U), u = (s.q_map / 3) % g.U;
     for (int i = 0; i < s.n_links;) {
       const AttnLink& lk = pl.links[s.link0 + i];
       const int r2 = lk.k_map / (3 * g.U);

@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           long long o_elem_i, lse_at_i;
           out_at(i, o_elem_i, lse_at_i);
           for (int k = 0; k < D / 8; ++k) {
-            if (p.o_bf16) {
+            if (s.o_bf16) {
               reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(s.o) + o_elem_i + 8 * k + cq)[0] = 0u;
             } else {
               reinterpret_cast<float2*>(static_cast<float*>(s.o) + o_elem_i + 8 * k + cq)[0] = make_float2(0.f, 0.f);
@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tc_fence_before();
           mbar_arrive(&o_empty[x]);
         }
-        if (p.o_bf16) {
+        if (s.o_bf16) {
           // The four threads of a row hold one bf16 pair of each 8-column group; a 4 x 4 word
           // transpose across them (two shuffle rounds) gives thread lane%4 all of groups
           // 4g + lane%4, which it writes as one 16-byte store per group.

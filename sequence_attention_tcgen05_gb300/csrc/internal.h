@@ -145,8 +145,9 @@ struct AttnLink {
 // and element (row * o_heads + h) * D of `o` (LSE: row * o_heads + h of `lse`); `o` and `lse` are
 // already offset to the run's first head.  Identity pos (o_len0 = INT_MAX) for a dense output.
 struct AttnSeg {
-  void* o;        // fp32 or bf16 per launch
+  void* o;        // bf16 when o_bf16, else fp32
   float* lse;     // may be null
+  int o_bf16;     // 1: bf16 O (a final output); 0: fp32 O (a final output or a ring partial)
   int q_map;
   int q_row0, q_len;
   int link0, n_links;
@@ -179,7 +180,6 @@ struct AttnParams {
   int n_segs;
   int n_units;
   int B;
-  int o_bf16;
   float scale_log2;
   uint32_t* status;
   unsigned long long budget_ns;

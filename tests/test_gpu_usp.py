@@ -68,6 +68,25 @@ def test_grid_small(U, R, order, mode, causal, monkeypatch):
     check_attention(o, l, ro, rl, f"grid U={U} R={R} {order} causal={causal} ring={mode}")
 
 
+@pytest.mark.parametrize("U,R,order,S,k", [
+    (1, 2, "contiguous", 1000, 1), (2, 2, "contiguous", 1537, 2), (1, 3, "stripe", 777, 1),
+    (2, 2, "zigzag", 1000, 1), (1, 4, "zigzag", 1537, 9), (3, 2, "contiguous", 2000, 3),
+])
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
+def test_split_fused_ring(U, R, order, S, k, out, monkeypatch):
+    """A fused non-causal ring with the last k 256-row blocks of its last ring chunk (last Ulysses
+    group) run as separate ring steps: their fp32 partials are merged after the attention, while
+    every other query block carries its chain (k = 9 splits the whole chunk)."""
+    monkeypatch.setenv("USP_RING_MERGE", "fused")
+    monkeypatch.setenv("USP_RING_SPLIT", str(k))
+    B, H, D = 1, max(2 * U, 4), 128
+    ws = usp.usp_attention_workspace_size(B, S, H, D, U, R, order, usp.USP_FP32, False)
+    assert ws > 256  # the split rows' partial slots
+    o, l, (qb, kb, vb) = run_usp(B, S, H, D, U, R, False, order, seed=S + k, out=out)
+    ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), 1 / math.sqrt(D), False)
+    check_attention(o, l, ro, rl, f"split fused ring U={U} R={R} {order} S={S} k={k} {out}")
+
+
 @pytest.mark.parametrize("mode", ["fused", "separate"])
 @pytest.mark.parametrize("B,S,H,D,U,R,causal", [
     (1, 512, 4, 64, 1, 2, True),      # half-chunks of 128 rows: one tile each
