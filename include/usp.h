@@ -208,9 +208,13 @@ usp_status_t usp_lse_merge(int n_parts, const float* o_parts, int64_t o_part_str
  *   The library picks the mode with the shorter modelled time (the merge pass and per-step
  *   epilogues against the load balance of fewer, longer units); the choice depends only on the
  *   arguments, so usp_attention_workspace_size and usp_attention agree.  USP_RING_MERGE=fused or
- *   =separate in the environment (read at each call) overrides it.  The head->seq re-layout and
- *   inverse reorder of O and LSE are the store addressing of (2) (one ring rank, or fused) or
- *   (3): the result lands in the global layout directly.
+ *   =separate in the environment (read at each call) overrides it.  A fused non-causal ring may
+ *   also run the last 256-row blocks of one ring chunk as separate ring steps, whose units are
+ *   dealt after all the chains and fill the last round of the launch, with their own partials
+ *   and (3) a merge over those rows only (USP_RING_SPLIT=0 never does, =k splits the last k
+ *   blocks of the last ring chunk; for tests).  The head->seq re-layout and inverse reorder of O
+ *   and LSE are the store addressing of (2) (one ring rank, or fused) or (3): the result lands
+ *   in the global layout directly.
  *   Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA as above. */
 usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
                            float scale, int causal, int ulysses_degree, int ring_degree,
@@ -222,10 +226,9 @@ usp_status_t usp_attention(const void* q, const void* k, const void* v, int B, i
  * attention functions, which outperform the unpacked ones): qkv is bf16 [B][S][3][H][D], i.e.
  * token t of batch b holds its query heads, then its key heads, then its value heads, in one row
  * of 3*H*D elements (the layout a fused QKV projection writes).  The attention's tensor maps read
- * the three tensors in place with a 3*H*D row stride, so nothing is unpacked; where usp_attention
- * copies Q, K, V into the workspace (zigzag chunks whose half-chunks are not whole 128-row tiles)
- * the copy reads the packed rows directly.  All other arguments, outputs, workspace and errors are
- * those of usp_attention (qkv must be 16-byte aligned). */
+ * the three tensors in place with a 3*H*D row stride, so nothing is unpacked.  All other
+ * arguments, outputs, workspace and errors are those of usp_attention (qkv must be 16-byte
+ * aligned). */
 usp_status_t usp_attention_qkvpacked(const void* qkv, int B, int S, int H, int D, float scale,
                                      int causal, int ulysses_degree, int ring_degree,
                                      const int32_t* seq_lens, const int32_t* head_counts,
@@ -280,7 +283,7 @@ usp_status_t usp_attention_noalloc(const void* q, const void* k, const void* v, 
 
 /* Bytes of workspace usp_attention needs for these arguments (0 on invalid arguments): a 256-byte
  * status word, plus ring_degree fp32 partial slots of O and LSE when the ring steps run
- * separately (see usp_attention). */
+ * separately, or for the split rows of a split fused ring (see usp_attention). */
 size_t usp_attention_workspace_size(int B, int S, int H, int D, int causal, int ulysses_degree,
                                     int ring_degree, usp_order_t order, usp_dtype_t o_dt);
 
