@@ -402,6 +402,41 @@ void add_links(const Grid& g, int r2, int u, int kv_len, int diag, int q_len,
   if (seen(n1, d1)) links.push_back({km, vm, g.span_off[r2], n1, d1});
 }
 
+// Causal pieces whose length is not a multiple of the 256-row block: cut the remainder off the
+// piece's start, so that the short block holds the rows that see the fewest keys (at the end it
+// would hold the rows that see the most, and cost as much as a whole block).  Chunks read
+// through a 5-D map have pieces of whole 128-row tiles, so the cut stays on a tile.
+void front_remainders(const Grid& g, std::vector<int>& cuts) {
+  if (!g.causal) return;
+  const size_t n = cuts.size();
+  for (size_t i = 0; i + 1 < n; ++i) {
+    const int len = cuts[i + 1] - cuts[i], rem = len % kAttnUnitRows;
+    if (len > kAttnUnitRows && rem != 0) cuts.push_back(cuts[i] + rem);
+  }
+  std::sort(cuts.begin(), cuts.end());
+}
+
+// The same for runs (separate ring steps): a run's remainder rows become a run of their own.
+std::vector<Run> front_remainders(const Grid& g, const std::vector<Run>& runs) {
+  if (!g.causal) return runs;
+  std::vector<Run> out;
+  for (const Run& run : runs) {
+    const int rem = run.q_len % kAttnUnitRows;
+    if (run.q_len > kAttnUnitRows && rem != 0) {
+      Run a = run, b = run;
+      a.q_len = rem;
+      b.q0 = run.q0 + rem;
+      b.q_len = run.q_len - rem;
+      if (b.diag != kNoDiag) b.diag += rem;
+      out.push_back(a);
+      out.push_back(b);
+    } else {
+      out.push_back(run);
+    }
+  }
+  return out;
+}
+
 // The runs of ring chunk r, cut where a span-mapped chunk's second half-chunk starts.
 std::vector<Run> cut_at_span(const Grid& g, int r, const std::vector<Run>& runs) {
   if (!g.span(r)) return runs;
@@ -429,7 +464,8 @@ usp_status_t plan_separate(const Grid& g, int oel, AttnPlan& pl) {
   for (int r = 0; r < g.R; ++r) {
     for (int kstep = 0; kstep < g.R; ++kstep) {
       const int r2 = (r - kstep + g.R) % g.R;
-      const std::vector<Run> runs = cut_at_span(g, r, plan_runs(g.pos[r], g.pos[r2], g.causal));
+      const std::vector<Run> runs =
+          front_remainders(g, cut_at_span(g, r, plan_runs(g.pos[r], g.pos[r2], g.causal)));
       for (const Run& run : runs)
         if (usp_status_t st = check_run_start(g, r, run)) return st;
       for (int u = 0; u < g.U; ++u) {
@@ -483,6 +519,7 @@ usp_status_t plan_fused(const Grid& g, int oel, AttnPlan& pl) {
     }
     std::sort(cuts.begin(), cuts.end());
     cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
+    front_remainders(g, cuts);
     for (size_t ci = 0; ci + 1 < cuts.size(); ++ci) {
       const int a = cuts[ci], b = cuts[ci + 1];
       for (int u = 0; u < g.U; ++u) {
