@@ -1309,7 +1309,9 @@ int usp_plan_chains(int S, int ulysses_degree, int ring_degree, int causal, usp_
       for (; j < s.n_links && pl.links[s.link0 + j].k_map == lk.k_map; ++j) kv_len += pl.links[s.link0 + j].kv_len;
       if (out && n < cap) {
         int32_t* rec = out + 8 * n;
-        rec[0] = u; rec[1] = r; rec[2] = s.o_row0; rec[3] = s.q_len;
+        // chunk-local first row (a split segment's o_row0 counts from the split row)
+        rec[0] = u; rec[1] = r; rec[2] = s.grp == g.U ? g.split_row + s.o_row0 : s.o_row0;
+        rec[3] = s.q_len;
         rec[4] = (r - r2 + g.R) % g.R; rec[5] = r2; rec[6] = kv_len; rec[7] = lk.diag;
       }
       ++n;

@@ -181,15 +181,23 @@ def test_planner_matches_oracle_visibility(L, S, U, R, causal, order):
         assert at == len(pos[r])
 
 
-@pytest.mark.parametrize("S,U,R,causal,order", [
-    (65536, 1, 8, True, "zigzag"), (61, 1, 5, True, "zigzag"), (61, 1, 4, True, "stripe"),
-    (7145, 2, 2, False, "contiguous"), (47, 2, 3, True, "stripe"), (19, 1, 8, True, "contiguous"),
-    (5, 1, 8, True, "zigzag"), (1537, 1, 3, True, "zigzag"), (1000, 1, 3, False, "zigzag"),
+@pytest.mark.parametrize("S,U,R,causal,order,split", [
+    (65536, 1, 8, True, "zigzag", ""), (61, 1, 5, True, "zigzag", ""), (61, 1, 4, True, "stripe", ""),
+    (7145, 2, 2, False, "contiguous", ""), (47, 2, 3, True, "stripe", ""), (19, 1, 8, True, "contiguous", ""),
+    (5, 1, 8, True, "zigzag", ""), (1537, 1, 3, True, "zigzag", ""), (1000, 1, 3, False, "zigzag", ""),
+    (32771, 1, 4, True, "stripe", ""), (65793, 1, 8, True, "zigzag", ""),
+    # forced splits of non-causal fused rings: the split rows' ring-step segments
+    (1000, 2, 2, False, "contiguous", "1"), (4481, 1, 3, False, "zigzag", "3"),
+    (1537, 2, 4, False, "stripe", "2"), (7145, 2, 2, False, "contiguous", "0"),
 ])
-def test_fused_chains_match_oracle_visibility(L, S, U, R, causal, order):
+def test_fused_chains_match_oracle_visibility(L, S, U, R, causal, order, split, monkeypatch):
     """The fused ring's pieces tile every ring chunk's query rows, each piece has at most one link
     per ring step, in ring order, and for every row the links' visible keys are exactly the keys
-    of that ring step's chunk that the oracle's global positions allow."""
+    of that ring step's chunk that the oracle's global positions allow (also for the rows of a
+    split fused ring, whose ring steps are separate segments)."""
+    monkeypatch.setenv("USP_RING_MERGE", "fused")
+    if split:
+        monkeypatch.setenv("USP_RING_SPLIT", split)
     pos = oracle.ring_positions(order, S, R)
     recs = usp.usp_plan_chains(S, U, R, causal, order)
     pieces = {}
