@@ -306,9 +306,9 @@ usp_status_t usp_check_status(void* status, usp_stream_t stream);
 
 /* Host-only planning query (no device needed): the chunk-pair work list usp_attention launches
  * when the ring steps run separately, for B = 1, as the causal pair schedule's runs (the launch
- * may cut a run further, at a zigzag chunk's half-chunk boundary or before a causal run's last
- * whole 256-row block, without changing which keys any row sees).  Writes up to `cap` records of
- * 8 int32 each into `out`:
+ * may cut a run further, at a zigzag chunk's half-chunk boundary or after a causal run's first
+ * (length mod 256) rows, without changing which keys any row sees).  Writes up to `cap` records
+ * of 8 int32 each into `out`:
  *   {ulysses index u, q ring chunk r, ring step k, kv ring chunk r2, q local row0, q rows,
  *    visible kv rows, diag}
  * where key c (0 <= c < visible kv rows, local to ring chunk r2) is visible to q local row i
