@@ -107,6 +107,25 @@ def test_plans_are_reused_and_follow_the_override(L, monkeypatch):
     assert L.usp_attention_workspace_size(*args) == 256
 
 
+def test_split_fused_ring_choice(L, monkeypatch):
+    """Qwen-Image 1328^2 over Ulysses 2 x ring 2 (non-causal, fused): 672 equal chains are 4.42
+    rounds of 152 CTAs, and the model splits the last 6 blocks (rows 2048..3571) of the second
+    ring chunk of the second Ulysses group into ring steps, whose fp32 partial slots are the
+    whole workspace beyond the status word; USP_RING_SPLIT=0 turns the split off."""
+    monkeypatch.delenv("USP_RING_MERGE", raising=False)
+    monkeypatch.delenv("USP_RING_SPLIT", raising=False)
+    args = (1, 7145, 24, 128, 2, 2, "contiguous", usp.USP_BF16, False)
+    vec = 1524 * 12  # split rows x heads of the group
+    align = lambda x: (x + 255) // 256 * 256
+    assert usp.usp_attention_ring_mode(1, 7145, 24, 128, False, 2, 2, "contiguous", usp.USP_BF16) == "fused"
+    assert usp.usp_attention_workspace_size(*args) == 256 + align(2 * vec * 128 * 4) + align(2 * vec * 4)
+    monkeypatch.setenv("USP_RING_SPLIT", "0")
+    assert usp.usp_attention_workspace_size(*args) == 256
+    # causal rings are never split
+    monkeypatch.delenv("USP_RING_SPLIT")
+    assert usp.usp_attention_workspace_size(1, 65536, 32, 128, 1, 8, "zigzag", usp.USP_BF16, True) == 256
+
+
 def test_workspace_size(L, monkeypatch):
     B, S, H, D = 1, 4608, 24, 128
     # contiguous Ulysses: Q/K/V are addressed in place and O is written in place -> status only
