@@ -4,12 +4,14 @@ synchronisation).  It runs on a 128 MiB scratch array built into the library ins
 workspace.
 
 This file is named to be collected last, so that a run stopping at its first failure has run every
-other test before these.  The GPU test calls the entry point through the C ABI three times in a
+other test before these.  The GPU test calls the entry point through the C ABI four times in a
 row on different problems and checks each result element by element against the fp64 oracle at
 the parity tests' tolerances.  The first two calls run the ring steps separately, so their fp32
 partials live in the shared scratch: the second call is causal with another ordering and grid, and
 its fully masked chunk pairs leave partial slots that it must not read, so anything it picked up
-from the first call's leftovers would show in its result.  The third call runs the fused ring."""
+from the first call's leftovers would show in its result.  The third call runs the fused ring,
+the fourth a fused ring with its last blocks split into ring steps (their partials in the
+scratch)."""
 import math
 
 import numpy as np
@@ -43,7 +45,7 @@ def _call_and_check(t, B, S, H, D, U, R, causal, order, out_dtype, seed):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_oracle_three_calls(monkeypatch):
+def test_noalloc_matches_oracle_four_calls(monkeypatch):
     import torch as t
     build.build_library()
     monkeypatch.setenv("USP_RING_MERGE", "separate")
@@ -54,6 +56,10 @@ def test_noalloc_matches_oracle_three_calls(monkeypatch):
     monkeypatch.setenv("USP_RING_MERGE", "fused")
     # ring of 4, zigzag, causal, fp32 out, fused ring steps
     _call_and_check(t, 2, 600, 3, 128, 1, 4, True, "zigzag", t.float32, seed=3)
+    # Ulysses 2 x ring 2, contiguous, non-causal, bf16 out: the last 2 blocks of the last ring
+    # chunk run as separate ring steps, merged from the scratch
+    monkeypatch.setenv("USP_RING_SPLIT", "2")
+    _call_and_check(t, 1, 1537, 4, 128, 2, 2, False, "contiguous", t.bfloat16, seed=4)
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(monkeypatch):
