@@ -68,18 +68,20 @@ def test_grid_small(U, R, order, mode, causal, monkeypatch):
     check_attention(o, l, ro, rl, f"grid U={U} R={R} {order} causal={causal} ring={mode}")
 
 
-@pytest.mark.parametrize("U,R,order,S,k", [
-    (1, 2, "contiguous", 1000, 1), (2, 2, "contiguous", 1537, 2), (1, 3, "stripe", 777, 1),
-    (2, 2, "zigzag", 1000, 1), (1, 4, "zigzag", 1537, 9), (3, 2, "contiguous", 2000, 3),
+@pytest.mark.parametrize("B,U,R,order,S,k", [
+    (1, 1, 2, "contiguous", 1000, 1), (1, 2, 2, "contiguous", 1537, 2), (1, 1, 3, "stripe", 777, 1),
+    (1, 2, 2, "zigzag", 1000, 1), (1, 1, 4, "zigzag", 1537, 9), (1, 3, 2, "contiguous", 2000, 3),
+    (2, 2, 2, "contiguous", 1100, 2), (2, 1, 3, "zigzag", 900, 1),
 ])
 @pytest.mark.parametrize("out", ["fp32", "bf16"])
-def test_split_fused_ring(U, R, order, S, k, out, monkeypatch):
+def test_split_fused_ring(B, U, R, order, S, k, out, monkeypatch):
     """A fused non-causal ring with the last k 256-row blocks of its last ring chunk (last Ulysses
     group) run as separate ring steps: their fp32 partials are merged after the attention, while
-    every other query block carries its chain (k = 9 splits the whole chunk)."""
+    every other query block carries its chain (k = 9 splits the whole chunk; B = 2 checks the
+    batch stride of the split rows' slots)."""
     monkeypatch.setenv("USP_RING_MERGE", "fused")
     monkeypatch.setenv("USP_RING_SPLIT", str(k))
-    B, H, D = 1, max(2 * U, 4), 128
+    H, D = max(2 * U, 4), 128
     ws = usp.usp_attention_workspace_size(B, S, H, D, U, R, order, usp.USP_FP32, False)
     assert ws > 256  # the split rows' partial slots
     o, l, (qb, kb, vb) = run_usp(B, S, H, D, U, R, False, order, seed=S + k, out=out)
