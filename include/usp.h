@@ -329,6 +329,26 @@ int usp_plan_pairs(int S, int ulysses_degree, int ring_degree, int causal, usp_o
 int usp_plan_chains(int S, int ulysses_degree, int ring_degree, int causal, usp_order_t order,
                     int32_t* out, int cap);
 
+/* Host-only planning query for the order of work units (no device needed): the attention
+ * launches usp_attention runs for these arguments (default seq_lens and head_counts) on a GPU
+ * with `sms` SMs.  Each launch runs one CTA per SM over its work units (one per head, batch and
+ * 256-row query block of a segment; numbered per Ulysses rank, head-major, longest first), and a
+ * deal fixes which CTA takes which unit.  By default a snake order: round t, CTA c takes unit
+ * t*G + c, or t*G + G-1-c for odd t (G CTAs).  A deal with (deal & 1) takes t*G + c in every
+ * round; one with (deal & 2) makes every odd (batch, head) index b * heads + h of a Ulysses rank
+ * visit its query blocks in reverse order.  The library models each deal's launch time (every
+ * unit costs its key tiles plus an epilogue of 2 tile periods for bf16 rows, 2.5 for fp32, on
+ * the CTA the deal gives it; the busiest CTA's total is the time) and keeps the fastest when it
+ * saves more than 1 % against the default.  The deal changes only the timing: each unit
+ * computes the same values wherever it runs.  USP_UNIT_DEAL=0..3 in the environment (read at
+ * each call) forces a deal.  Writes up to `cap` records of 4 int32 each into `out`, one per
+ * launch:
+ *   {work units, deal, modelled time of that deal, modelled time of the default deal}
+ * with times in thousandths of a key-tile period.  Returns the launch count (which may exceed
+ * cap), or -1 on invalid arguments (sms < 1, or as usp_attention_ring_mode). */
+int usp_plan_deals(int B, int S, int H, int D, int causal, int ulysses_degree, int ring_degree,
+                   usp_order_t order, usp_dtype_t o_dt, int sms, int32_t* out, int cap);
+
 const char* usp_status_string(usp_status_t s);
 const char* usp_last_error(void);
 int usp_version(void); /* major*10000 + minor*100 + patch */

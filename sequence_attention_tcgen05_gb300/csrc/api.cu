@@ -2,6 +2,7 @@
 // launch sequence of usp_attention.  Nothing here allocates device memory or synchronises,
 // except usp_check_status.
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -702,12 +703,12 @@ void choose_split(Grid& g, usp_dtype_t o_dt) {
 // plans are kept.
 // ------------------------------------------------------------------------------------------------
 struct PlanKey {
-  int B, S, H, D, causal, U, R, order, o_dt, ring_env, split_env;
+  int B, S, H, D, causal, U, R, order, o_dt, ring_env, split_env, deal_env;
   std::vector<int32_t> seq_lens, head_counts;
   bool operator==(const PlanKey& o) const {
     return B == o.B && S == o.S && H == o.H && D == o.D && causal == o.causal && U == o.U &&
            R == o.R && order == o.order && o_dt == o.o_dt && ring_env == o.ring_env &&
-           split_env == o.split_env &&
+           split_env == o.split_env && deal_env == o.deal_env &&
            seq_lens == o.seq_lens && head_counts == o.head_counts;
   }
 };
@@ -727,7 +728,7 @@ usp_status_t get_plan(int B, int S, int H, int D, int causal, int U, int R, usp_
                       const int32_t* seq_lens, const int32_t* head_counts, usp_dtype_t o_dt,
                       std::shared_ptr<const PlanEntry>& out) {
   PlanKey key{B, S, H, D, causal != 0, U, R, static_cast<int>(order), static_cast<int>(o_dt), ring_env(),
-              split_env(), {}, {}};
+              split_env(), deal_env(), {}, {}};
   if (seq_lens && U >= 1 && R >= 1 && U <= 16 && R <= 16) key.seq_lens.assign(seq_lens, seq_lens + U * R);
   if (head_counts && U >= 1 && U <= 16) key.head_counts.assign(head_counts, head_counts + U);
   {
@@ -1246,6 +1247,36 @@ int usp_attention_ring_mode(int B, int S, int H, int D, int causal, int ulysses_
   if (get_plan(B, S, H, D, causal, ulysses_degree, ring_degree, order, nullptr, nullptr, o_dt, pe) != USP_OK)
     return -1;
   return pe->g.R == 1 ? 0 : (pe->g.fused_ring ? 2 : 1);
+}
+
+int usp_plan_deals(int B, int S, int H, int D, int causal, int ulysses_degree, int ring_degree,
+                   usp_order_t order, usp_dtype_t o_dt, int sms, int32_t* out, int cap) {
+  if (sms < 1) {
+    fail(USP_ERR_INVALID_ARG, "need sms >= 1");
+    return -1;
+  }
+  std::shared_ptr<const PlanEntry> pe;
+  if (get_plan(B, S, H, D, causal, ulysses_degree, ring_degree, order, nullptr, nullptr, o_dt, pe) != USP_OK)
+    return -1;
+  std::vector<AttnSeg> segs = pe->plan.segs;
+  for (size_t i = 0; i < segs.size(); ++i) segs[i].o_bf16 = !pe->plan.outs[i].partial && o_dt == USP_BF16;
+  AttnParams base;
+  std::memset(&base, 0, sizeof(base));
+  base.B = B;
+  base.scale_log2 = 1.f;
+  std::vector<AttnLaunch> launches;
+  if (pack_attention(base, segs, pe->plan.links, launches, sms) != USP_OK) return -1;
+  const int n = static_cast<int>(launches.size());
+  for (int i = 0; i < n && out && i < cap; ++i) {
+    const AttnParams& p = launches[i].params;
+    const int ctas = std::max(1, std::min(p.n_units, sms));
+    int32_t* rec = out + 4 * i;
+    rec[0] = p.n_units;
+    rec[1] = p.deal;
+    rec[2] = static_cast<int32_t>(std::lround(1000.0 * deal_periods(p, p.deal, ctas)));
+    rec[3] = static_cast<int32_t>(std::lround(1000.0 * deal_periods(p, 0, ctas)));
+  }
+  return n;
 }
 
 usp_status_t usp_check_status(void* status, usp_stream_t stream) {

@@ -61,6 +61,7 @@
 // Every mbarrier wait is bounded (see ptx.cuh); on a timeout all roles stop, drain their
 // in-flight copies and MMAs, free TMEM and exit, and the status word records the error.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 
 #include "internal.h"
@@ -114,7 +115,7 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
   const AttnGroup& G = p.groups[gl];
   const int local = unit - G.unit0;
   const int hb = local / G.blocks;
-  const int rem = local - hb * G.blocks;  // block index within the group's segments
+  const int rem = deal_block(local - hb * G.blocks, G.blocks, hb, p.deal);  // over the segments
   int lo = G.seg0, hi = G.seg0 + G.n_segs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -137,13 +138,13 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
   return u;
 }
 
-// Units are dealt to the CTAs in a snake order: in round t CTA c takes unit t*G + c for even t and
-// t*G + G-1-c for odd t.  The host lists units longest first, so each CTA's total stays close to
-// the mean (a longest-processing-time deal) while neighbouring CTAs still work on the same head's
-// K/V at the same time, which keeps those tiles in L2.  Every role walks the same sequence.
-__device__ __forceinline__ int unit_of_round(int t) {
-  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  return t * G + ((t & 1) ? G - 1 - c : c);
+// The unit this CTA takes in round t under the launch's deal.  By default the snake order: in
+// round t CTA c takes unit t*G + c for even t and t*G + G-1-c for odd t.  The host lists units
+// longest first, so each CTA's total stays close to the mean (a longest-processing-time deal)
+// while neighbouring CTAs still work on the same head's K/V at the same time, which keeps those
+// tiles in L2.  Every role walks the same sequence.
+__device__ __forceinline__ int unit_of_round(const AttnParams& p, int t) {
+  return deal_unit(t, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), p.deal);
 }
 
 // Max over one row's 32 values of a 16x256b.x16 load (registers 4k + 2i + {0,1}, k < 16), then
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int s = 0; s < STAGES; ++s) kfills[s] = vfills[s] = 0;
       const int rounds = p.withhold_loads ? 0 : (p.n_units + gridDim.x - 1) / gridDim.x;
       for (int t = 0; t < rounds; ++t) {
-        const int unit = unit_of_round(t);
+        const int unit = unit_of_round(p, t);
         if (unit >= p.n_units) continue;
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       };
       const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
       for (int t = 0; t < rounds && ok; ++t) {
-        const int unit = unit_of_round(t);
+        const int unit = unit_of_round(p, t);
         if (unit >= p.n_units) continue;
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     };
     const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
     for (int t = 0; t < rounds && ok; ++t) {
-      const int unit = unit_of_round(t);
+      const int unit = unit_of_round(p, t);
       if (unit >= p.n_units) continue;
       const Unit u = decode_unit(p, unit);
       const AttnSeg& s = *u.seg;
@@ -785,8 +786,40 @@ usp_status_t make_qkv_map(CUtensorMap* map, const void* base, int n_heads, int D
   return USP_OK;
 }
 
+int deal_env() {
+  const char* env = std::getenv("USP_UNIT_DEAL");
+  if (!env || !*env) return -1;
+  return std::atoi(env) & (kDealCount - 1);
+}
+
+double deal_periods(const AttnParams& p, int deal, int ctas) {
+  std::vector<double> load(ctas, 0.0), cost;
+  for (int gi = 0; gi < p.n_groups; ++gi) {
+    const AttnGroup& G = p.groups[gi];
+    cost.clear();  // key tiles + epilogue of every block of the group, in block order
+    for (int si = G.seg0; si < G.seg0 + G.n_segs; ++si) {
+      const AttnSeg& s = p.segs[si];
+      for (int qi = 0; qi < s.n_qblk; ++qi) {
+        const int qb = s.rev ? s.n_qblk - 1 - qi : qi;
+        const int last = std::min(s.q_len, (qb + 1) * kAttnUnitRows) - 1;
+        int n = 0;
+        for (int l = 0; l < s.n_links; ++l) n += link_tiles(p.links[s.link0 + l], last);
+        cost.push_back(n + (s.o_bf16 ? 2.0 : 2.5));
+      }
+    }
+    const int n = G.blocks * p.segs[G.seg0].n_heads * p.B;
+    for (int i = 0; i < n; ++i) {
+      const int unit = G.unit0 + i, t = unit / ctas;
+      const int hb = i / G.blocks;
+      load[deal_unit(t, unit - t * ctas, ctas, deal) - t * ctas] +=
+          cost[deal_block(i - hb * G.blocks, G.blocks, hb, deal)];
+    }
+  }
+  return *std::max_element(load.begin(), load.end());
+}
+
 usp_status_t pack_attention(const AttnParams& base, std::vector<AttnSeg>& segs,
-                            const std::vector<AttnLink>& links, std::vector<AttnLaunch>& out) {
+                            const std::vector<AttnLink>& links, std::vector<AttnLaunch>& out, int sms) {
   out.clear();
   if (!(base.scale_log2 > 0.f)) return fail(USP_ERR_INVALID_ARG, "the softmax scale must be positive");
   // Segments grouped by unit group, longest first within a group: sort by the key tiles their
@@ -839,6 +872,19 @@ usp_status_t pack_attention(const AttnParams& base, std::vector<AttnSeg>& segs,
     p.n_segs = used;
     p.n_groups = n_groups;
     p.n_units = static_cast<int>(units);
+    // the unit deal with the shortest modelled launch, if it beats the default by more than 1 %
+    p.deal = 0;
+    if (const int forced = deal_env(); forced >= 0) {
+      p.deal = forced;
+    } else if (units > 0) {
+      const int ctas = std::max(1, std::min(p.n_units, sms > 0 ? sms : sm_count()));
+      const double t0 = deal_periods(p, 0, ctas);
+      double best = t0;
+      for (int d = 1; d < kDealCount; ++d) {
+        const double t = deal_periods(p, d, ctas);
+        if (t < best && t < 0.99 * t0) { best = t; p.deal = d; }
+      }
+    }
     // the mask-free kernel when every link is whole key tiles without a causal diagonal
     L.masks = false;
     for (int i = 0; i < n_links; ++i)

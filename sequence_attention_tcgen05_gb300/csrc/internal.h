@@ -170,6 +170,27 @@ struct AttnGroup {
   int seg0, n_segs;
 };
 
+// Unit deals: which CTA of a G-CTA grid takes which unit, and in which order each (batch, head)
+// of a group visits its blocks.  Every role of the kernel walks the same sequence, and each unit
+// computes the same values wherever it runs, so the deal changes timing only.
+//   default: snake order (round t: CTA c takes unit t*G + c, or t*G + G-1-c for odd t), every
+//            (batch, head) visiting its blocks in the group's order (longest first);
+//   kDealRoundRobin: round t, CTA c takes unit t*G + c;
+//   kDealAlternate:  odd (batch, head) indices of a group visit their blocks in reverse order.
+constexpr int kDealRoundRobin = 1;
+constexpr int kDealAlternate = 2;
+constexpr int kDealCount = 4;
+// The unit CTA c takes in round t (the map is its own inverse within a round: the CTA that takes
+// unit u is deal_unit(u / G, u % G, G, deal) - (u / G) * G).
+__host__ __device__ inline int deal_unit(int t, int c, int G, int deal) {
+  const bool flip = !(deal & kDealRoundRobin) && (t & 1);
+  return t * G + (flip ? G - 1 - c : c);
+}
+// The block (index over the group's segments) that a (batch, head) index hb visits rem-th.
+__host__ __device__ inline int deal_block(int rem, int blocks, int hb, int deal) {
+  return (deal & kDealAlternate) && (hb & 1) ? blocks - 1 - rem : rem;
+}
+
 struct AttnParams {
   CUtensorMap maps[kAttnMaxMaps];
   int map_rows[kAttnMaxMaps];  // two-piece maps: rows per piece (row l = piece l / n, row l % n); 0: one piece
@@ -179,6 +200,7 @@ struct AttnParams {
   int n_groups;
   int n_segs;
   int n_units;
+  int deal;            // kDealRoundRobin | kDealAlternate bits
   int B;
   float scale_log2;
   uint32_t* status;
@@ -210,9 +232,18 @@ struct AttnLaunch {
   bool masks;
 };
 // Packs the segments (sorted in place) and their links into launches, each starting from `base`
-// (maps, scale, status, budget); then runs them.
+// (maps, scale, status, budget), with the unit deal chosen for a grid of min(units, sms) CTAs
+// (sms = 0: the current device's SM count); run_attention runs them.
 usp_status_t pack_attention(const AttnParams& base, std::vector<AttnSeg>& segs,
-                            const std::vector<AttnLink>& links, std::vector<AttnLaunch>& out);
+                            const std::vector<AttnLink>& links, std::vector<AttnLaunch>& out,
+                            int sms = 0);
+// Modelled time of one packed launch over `ctas` CTAs in key-tile periods under a unit deal: each
+// unit costs its key tiles plus an epilogue (2 periods for bf16 rows, 2.5 for fp32) and runs on
+// the CTA the deal gives it.  pack_attention gives each launch the deal with the shortest
+// modelled time when it beats the default by more than 1 %; USP_UNIT_DEAL=0..3 in the
+// environment (read at each call) forces one.
+double deal_periods(const AttnParams& p, int deal, int ctas);
+int deal_env();  // -1 when USP_UNIT_DEAL is unset
 usp_status_t run_attention(const std::vector<AttnLaunch>& launches, int D, cudaStream_t stream);
 
 // Launch over all segments, each with its own links (split into several launches if there are

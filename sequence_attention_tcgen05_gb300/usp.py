@@ -24,7 +24,8 @@ EXPORTED = [
     "usp_attention_noalloc",
     "usp_attention_workspace_size", "usp_attention_ring_mode",
     "usp_check_status",
-    "usp_plan_pairs", "usp_plan_chains", "usp_status_string", "usp_last_error", "usp_version",
+    "usp_plan_pairs", "usp_plan_chains", "usp_plan_deals", "usp_status_string", "usp_last_error",
+    "usp_version",
 ]
 
 
@@ -90,6 +91,7 @@ def lib() -> ctypes.CDLL:
         "usp_check_status": [vp, vp],
         "usp_plan_pairs": [i32, i32, i32, i32, i32, i32p, i32],
         "usp_plan_chains": [i32, i32, i32, i32, i32, i32p, i32],
+        "usp_plan_deals": [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32p, i32],
         "usp_status_string": [i32],
         "usp_last_error": [],
         "usp_version": [],
@@ -303,6 +305,20 @@ def usp_plan_chains(S, ulysses_degree, ring_degree, causal, order="contiguous"):
     buf = (ctypes.c_int32 * (8 * max(1, n)))()
     lib().usp_plan_chains(S, ulysses_degree, ring_degree, int(causal), ORDERS[order], buf, n)
     return [tuple(buf[8 * i: 8 * i + 8]) for i in range(n)]
+
+
+def usp_plan_deals(B, S, H, D, causal, ulysses_degree, ring_degree, order="contiguous",
+                   o_dt=USP_BF16, sms=152):
+    """Per attention launch: (work units, deal, modelled periods of that deal, modelled periods of
+    the default deal), periods as floats."""
+    args = (B, S, H, D, int(causal), ulysses_degree, ring_degree, ORDERS[order], o_dt, sms)
+    n = lib().usp_plan_deals(*args, None, 0)
+    if n < 0:
+        raise UspError(USP_ERR_INVALID_ARG, "usp_plan_deals", lib().usp_last_error().decode())
+    buf = (ctypes.c_int32 * (4 * max(1, n)))()
+    lib().usp_plan_deals(*args, buf, n)
+    return [(buf[4 * i], buf[4 * i + 1], buf[4 * i + 2] / 1000.0, buf[4 * i + 3] / 1000.0)
+            for i in range(n)]
 
 
 def usp_version() -> int:

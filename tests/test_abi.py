@@ -267,3 +267,81 @@ def test_binding_signatures_match_header(L):
         assert m, name
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(getattr(L, name).argtypes) == len(params), name
+
+
+def modelled_deal_periods(B, S, H, U, R, causal, order, bf16, deal, sms=152):
+    """The unit-deal time model restated from the header over the fused ring's pieces: per Ulysses
+    rank, the pieces longest first (by the key tiles of their longest block), every (batch, head)
+    visiting their 256-row blocks in order (causal: last block first), reversed for odd (batch,
+    head) indices under deal & 2; unit i goes to CTA i % G in even rounds and, unless deal & 1,
+    to G-1 - i % G in odd ones; a unit costs its key tiles + 2 (bf16 O) or 2.5 (fp32 O)."""
+    pieces = {}
+    for (u, r, row0, rows, k, r2, kvlen, diag) in usp.usp_plan_chains(S, U, R, causal, order):
+        pieces.setdefault((u, r, row0, rows), []).append((kvlen, diag))
+
+    def tiles(links, last):
+        n = 0
+        for kv, diag in links:
+            m = kv - 1 if diag == INT32_MAX else min(kv - 1, last + diag)
+            n += 0 if m < 0 else m // 128 + 1
+        return n
+
+    units = []
+    for u in range(U):
+        mine = sorted(((key[3], links) for key, links in pieces.items() if key[0] == u),
+                      key=lambda p: -tiles(p[1], p[0] - 1))
+        blocks = []
+        for rows, links in mine:
+            nb = -(-rows // 256)
+            for qi in range(nb):
+                qb = nb - 1 - qi if causal else qi
+                blocks.append(tiles(links, min(rows, 256 * (qb + 1)) - 1) + (2.0 if bf16 else 2.5))
+        for hb in range(B * H // U):
+            units += blocks[::-1] if (deal & 2) and hb % 2 else blocks
+    ctas = min(len(units), sms)
+    load = [0.0] * ctas
+    for i, c in enumerate(units):
+        t, pos = divmod(i, ctas)
+        load[ctas - 1 - pos if not (deal & 1) and t % 2 else pos] += c
+    return max(load)
+
+
+@pytest.mark.parametrize("B,S,H,U,R,causal,order", [
+    (1, 65536, 32, 1, 8, True, "zigzag"), (2, 1085, 3, 1, 4, True, "contiguous"),
+    (2, 1536, 3, 1, 3, True, "zigzag"), (1, 32771, 32, 1, 4, True, "stripe"),
+    (1, 12289, 4, 1, 2, True, "contiguous"), (2, 4481, 6, 2, 2, True, "stripe"),
+    (1, 7145, 24, 2, 2, False, "contiguous"), (3, 3000, 10, 2, 3, False, "stripe"),
+])
+def test_unit_deal_model(L, B, S, H, U, R, causal, order, monkeypatch):
+    """usp_plan_deals against the model restated over usp_plan_chains for every deal (forced with
+    USP_UNIT_DEAL), and the library's own pick: the deal of least modelled time when it saves
+    more than 1 % against the default, else the default."""
+    monkeypatch.setenv("USP_RING_MERGE", "fused")
+    monkeypatch.setenv("USP_RING_SPLIT", "0")
+    for bf16 in (False, True):
+        dt = usp.USP_BF16 if bf16 else usp.USP_FP32
+        want = [modelled_deal_periods(B, S, H, U, R, causal, order, bf16, d) for d in range(4)]
+        for d in range(4):
+            monkeypatch.setenv("USP_UNIT_DEAL", str(d))
+            ((n, deal, t, t0),) = usp.usp_plan_deals(B, S, H, 128, causal, U, R, order, dt)
+            assert deal == d and abs(t - want[d]) < 1e-3 and abs(t0 - want[0]) < 1e-3, (d, t, want)
+        monkeypatch.delenv("USP_UNIT_DEAL")
+        ((n, deal, t, t0),) = usp.usp_plan_deals(B, S, H, 128, causal, U, R, order, dt)
+        better = [d for d in range(1, 4) if want[d] < 0.99 * want[0]]
+        assert deal == (min(better, key=lambda d: (want[d], d)) if better else 0)
+        assert abs(t - want[deal]) < 1e-3
+
+
+def test_unit_deal_choices(L, monkeypatch):
+    """The 65793-token causal zigzag ring over 8 ranks gets a deal other than the default (its
+    zigzag half-chunks of 4112 and 4112.125 rows leave blocks of very unequal cost across the
+    heads), saving more than 1 % of the modelled launch; the 64K ring keeps the snake order; the
+    query rejects a GPU without SMs."""
+    for var in ("USP_UNIT_DEAL", "USP_RING_MERGE", "USP_RING_SPLIT"):
+        monkeypatch.delenv(var, raising=False)
+    ((n, deal, t, t0),) = usp.usp_plan_deals(1, 65793, 32, 128, True, 1, 8, "zigzag")
+    assert deal != 0 and t < 0.99 * t0
+    ((n, deal, t, t0),) = usp.usp_plan_deals(1, 65536, 32, 128, True, 1, 8, "zigzag")
+    assert n == 8192 and deal == 0 and t == t0
+    with pytest.raises(usp.UspError):
+        usp.usp_plan_deals(1, 65536, 32, 128, True, 1, 8, "zigzag", sms=0)

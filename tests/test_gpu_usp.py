@@ -289,3 +289,34 @@ def test_repeated_calls_on_the_same_buffers(monkeypatch):
         assert usp.usp_check_status(ws) == usp.USP_OK
         ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), scale, True)
         check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl, f"repeat seed={seed} ring={mode}")
+
+
+@pytest.mark.parametrize("B,S,H,D,U,R,causal,order,split,deal", [
+    (2, 1570, 3, 64, 1, 3, True, "zigzag", None, 1),       # round-robin beats the snake
+    (2, 600, 3, 64, 1, 4, True, "zigzag", None, 2),        # odd heads visit their blocks in reverse
+    (2, 1085, 3, 64, 1, 4, True, "contiguous", None, 3),   # both
+    (1, 3000, 16, 64, 1, 4, True, "stripe", None, 0),
+    (1, 2600, 16, 128, 2, 2, False, "contiguous", 2, 0),   # split fused ring: a second unit group
+])
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
+def test_unit_deals_bit_identical(B, S, H, D, U, R, causal, order, split, deal, out, monkeypatch):
+    """The deal (which CTA takes which work unit, and in which order each head visits its query
+    blocks) changes only the timing: every forced deal gives the bits of the library's own
+    choice, which is the one its time model names and matches the oracle.  Every case has more
+    units than a GB300 has SMs, so the deals differ from the second round on."""
+    monkeypatch.delenv("USP_UNIT_DEAL", raising=False)
+    if split is not None:
+        monkeypatch.setenv("USP_RING_SPLIT", str(split))
+    o_dt = usp.USP_FP32 if out == "fp32" else usp.USP_BF16
+    chosen = usp.usp_plan_deals(B, S, H, D, causal, U, R, order, o_dt)
+    assert [d for _, d, _, _ in chosen] == [deal] and chosen[0][0] > 152
+    o, l, (qb, kb, vb) = run_usp(B, S, H, D, U, R, causal, order, seed=31, out=out)
+    for forced in range(4):
+        monkeypatch.setenv("USP_UNIT_DEAL", str(forced))
+        assert [d for _, d, _, _ in usp.usp_plan_deals(B, S, H, D, causal, U, R, order, o_dt)] == \
+            [forced] * len(chosen)
+        o2, l2, _ = run_usp(B, S, H, D, U, R, causal, order, seed=31, out=out)
+        assert np.array_equal(o2.view(np.uint32), o.view(np.uint32)), forced
+        assert np.array_equal(l2.view(np.uint32), l.view(np.uint32)), forced
+    ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), 1 / math.sqrt(D), causal)
+    check_attention(o, l, ro, rl, f"deal {chosen} {order} causal={causal} out={out}")
