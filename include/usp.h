@@ -189,7 +189,11 @@ usp_status_t usp_lse_merge(int n_parts, const float* o_parts, int64_t o_part_str
  *   o: [B][S][H][D] of o_dt; lse: fp32 [B][S][H] or NULL.
  *   workspace: device scratch of at least usp_attention_workspace_size(...) bytes, 256-byte
  *   aligned.  Its first 4 bytes are the status word usp_check_status reads and clears; zero
- *   them once before the first call (e.g. allocate the workspace zeroed).
+ *   them once before the first call (e.g. allocate the workspace zeroed).  Bytes 8-15 hold the
+ *   counter of a dynamic unit deal (see usp_plan_deals): every launch that uses it leaves it
+ *   zero when it ends, and the library clears it in the stream whenever a thread calls with a
+ *   workspace, plan or buffers other than its previous call's.  Leave bytes 0-15 to the library
+ *   between calls.
  *   Steps (one stream): (1) the seq->head re-layout of Q, K, V (with the ring ordering) is
  *   addressing, not a pass: each virtual rank's head-sharded view is read in place by the
  *   attention's tensor maps, one map over its ring chunk when that is one affine run of global
@@ -335,14 +339,17 @@ int usp_plan_chains(int S, int ulysses_degree, int ring_degree, int causal, usp_
  * 256-row query block of a segment; numbered per Ulysses rank, head-major, longest first), and a
  * deal fixes which CTA takes which unit.  By default a snake order: round t, CTA c takes unit
  * t*G + c, or t*G + G-1-c for odd t (G CTAs).  A deal with (deal & 1) takes t*G + c in every
- * round; one with (deal & 2) makes every odd (batch, head) index b * heads + h of a Ulysses rank
- * visit its query blocks in reverse order.  The library models each deal's launch time (every
- * unit costs its key tiles plus an epilogue of 2 tile periods for bf16 rows, 2.5 for fp32, on
- * the CTA the deal gives it; the busiest CTA's total is the time) and keeps the fastest when it
- * saves more than 1 % against the default.  The deal changes only the timing: each unit
- * computes the same values wherever it runs.  USP_UNIT_DEAL=0..3 in the environment (read at
- * each call) forces a deal.  Writes up to `cap` records of 4 int32 each into `out`, one per
- * launch:
+ * round; one with (deal & 4) is dynamic: each CTA takes the next unit in numbering order from a
+ * counter in the workspace when it is ready for one; one with (deal & 2) makes every odd
+ * (batch, head) index b * heads + h of a Ulysses rank visit its query blocks in reverse order.
+ * The library models each deal's launch time (every unit costs its key tiles plus an epilogue of
+ * 2 tile periods for bf16 rows, 2.5 for fp32; static deals put it on the CTA the deal names,
+ * the dynamic one on the CTA free first, the lowest index among equals; the busiest CTA's total
+ * is the time) and keeps the fastest when it saves more than 0.5 % against the default.  The deal
+ * changes only the timing: each unit computes the same values wherever it runs.
+ * USP_UNIT_DEAL=0..7 in the environment (read at each call) forces a deal (usp_attn_partial,
+ * which has no workspace, drops the dynamic bit).  Writes up to `cap` records of 4 int32 each
+ * into `out`, one per launch:
  *   {work units, deal, modelled time of that deal, modelled time of the default deal}
  * with times in thousandths of a key-tile period.  Returns the launch count (which may exceed
  * cap), or -1 on invalid arguments (sms < 1, or as usp_attention_ring_mode). */

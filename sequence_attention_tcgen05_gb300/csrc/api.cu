@@ -1062,6 +1062,7 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
   const unsigned long long budget = wait_budget_ns();
   const int withhold = withhold_loads();
   const bool partials = R > 1 && !g.fused_ring;
+  bool clear_counter = false;
   if (!(memo.pe == pe && memo.q == q && memo.k == k && memo.v == v && memo.o == o &&
         memo.lse == lse && memo.ws == workspace && memo.in_rs == in_rs && memo.scale == scale &&
         memo.budget == budget && memo.withhold == withhold)) {
@@ -1100,6 +1101,7 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     p.B = B;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = reinterpret_cast<uint32_t*>(ws);
+    p.counter = reinterpret_cast<uint32_t*>(ws) + 2;  // bytes 8-15: the dynamic deal's counter
     p.budget_ns = budget;
     p.withhold_loads = withhold;
     // the cached plan's segments, bound to this call's output and workspace
@@ -1119,6 +1121,14 @@ static usp_status_t attention_impl(const void* q, const void* k, const void* v, 
     memo.pe = pe;
     memo.q = q; memo.k = k; memo.v = v; memo.o = o; memo.lse = lse; memo.ws = workspace;
     memo.in_rs = in_rs; memo.scale = scale; memo.budget = budget; memo.withhold = withhold;
+    for (const AttnLaunch& L : memo.launches) clear_counter = clear_counter || (L.params.deal & kDealDynamic);
+  }
+  // A dynamic deal's counter returns to zero at the end of every launch; it is set to zero here
+  // whenever this thread binds a new plan or workspace, so a workspace whose bytes 8-15 were not
+  // zeroed still starts from zero.
+  if (clear_counter) {
+    const cudaError_t e = cudaMemsetAsync(ws + 8, 0, 8, stream);
+    if (e != cudaSuccess) return fail(USP_ERR_CUDA, "clearing the unit counter: %s", cudaGetErrorString(e));
   }
   if ((st = mark(0))) return st;
 
@@ -1264,6 +1274,8 @@ int usp_plan_deals(int B, int S, int H, int D, int causal, int ulysses_degree, i
   std::memset(&base, 0, sizeof(base));
   base.B = B;
   base.scale_log2 = 1.f;
+  static uint32_t no_counter[2];  // usp_attention has a counter, so dynamic deals are allowed; never read
+  base.counter = no_counter;
   std::vector<AttnLaunch> launches;
   if (pack_attention(base, segs, pe->plan.links, launches, sms) != USP_OK) return -1;
   const int n = static_cast<int>(launches.size());

@@ -63,6 +63,10 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -80,6 +84,10 @@ constexpr uint32_t kRegsLaunch = 96;
 constexpr uint32_t kRegsWG0 = 56;
 constexpr uint32_t kRegsSoftmax = 104;
 static_assert(128 * kRegsWG0 + 512 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+// Dynamic deal: slots of the unit queue from the producer thread to the other roles, and the
+// warps that read each slot (the MMA warp and the 16 softmax warps).
+constexpr int kUnitQ = 4;
+constexpr int kUnitReaders = 1 + (kThreads - 128) / 32;
 
 template <int D, int STAGES>
 struct Layout {
@@ -93,7 +101,9 @@ struct Layout {
   // q_full, q_empty, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2],
   // pv_done[2], o_empty[2], mma_done
   static constexpr int kNumBars = 2 + 4 * STAGES + 9;
-  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  // unit queue: full[kUnitQ], empty[kUnitQ] barriers, then int[kUnitQ] slots
+  static constexpr int kUnitQueue = kBar + kNumBars * 8;
+  static constexpr int kTmemSlot = kUnitQueue + 2 * kUnitQ * 8 + 4 * kUnitQ;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kAlloc = kEnd + 1024;  // slack to align the base to 1024 B
@@ -145,6 +155,88 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, int unit) {
 // tiles in L2.  Every role walks the same sequence.
 __device__ __forceinline__ int unit_of_round(const AttnParams& p, int t) {
   return deal_unit(t, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), p.deal);
+}
+
+// Under the dynamic deal the producer thread takes each next unit from the launch's counter in
+// global memory (units in their numbering order, each to the CTA that asks first) and passes it
+// to the MMA warp and the softmax warps through a kUnitQ-slot queue in shared memory: `full[s]`
+// completes when the producer has written slot s, `empty[s]` when every reading warp has read
+// it.  A unit index >= n_units ends the walk.  Under a static deal every role computes its k-th
+// unit alone.
+
+// Shared-memory address OFF bytes into the kernel's 1024-aligned shared memory (the unit queue:
+// full[kUnitQ], empty[kUnitQ] barriers, then kUnitQ int slots; or the abort flag), recomputed
+// from the dynamic shared memory base where it is used so that no register holds it across a
+// role's unit loop.
+template <int OFF>
+__device__ __forceinline__ uint32_t shared_at() {
+  extern __shared__ uint8_t smem_raw[];
+  return ((smem_u32(smem_raw) + 1023u) & ~1023u) + OFF;
+}
+__device__ __forceinline__ uint32_t uq_full(uint32_t q, int s) { return q + 8 * s; }
+__device__ __forceinline__ uint32_t uq_empty(uint32_t q, int s) { return q + 8 * (kUnitQ + s); }
+__device__ __forceinline__ uint32_t uq_slot(uint32_t q, int s) { return q + 16 * kUnitQ + 4 * s; }
+
+// The producer thread's k-th unit; false if a wait gave up.
+template <int OFF>
+__device__ __forceinline__ bool produce_unit(const AttnParams& p, int k, volatile int* abort_flag,
+                                             uint64_t budget, int& unit) {
+  if (!(p.deal & kDealDynamic)) {
+    unit = unit_of_round(p, k);
+    return true;
+  }
+  const uint32_t q = shared_at<OFF>();
+  const int s = k & (kUnitQ - 1);
+  if (k >= kUnitQ && !mbar_wait_at(uq_empty(q, s), ((k / kUnitQ) - 1) & 1, abort_flag, p.status, budget))
+    return false;
+  unit = static_cast<int>(atomicAdd(p.counter, 1u));
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(uq_slot(q, s)), "r"(unit) : "memory");
+  mbar_arrive_at(uq_full(q, s));  // release: the slot's value is visible to whoever waits on it
+  return true;
+}
+
+// Wait of the softmax warps for a queue slot, lighter than mbar_wait (their registers are all
+// taken across the unit loop): the abort flag is read through its shared address, and instead
+// of a clock the wait counts its polls.  The producer fills each slot well before the softmax
+// warps get to it (after issuing the loads of the unit before, while the MMA warp and the
+// softmax are still on that unit), and the MMA warp waits for the same slot with a timed wait
+// that raises the abort flag, so the count only bounds a failure: after 2^22 polls the wait
+// raises the abort flag and the timeout status itself.
+__device__ __forceinline__ bool queue_wait_polls(uint32_t bar, uint32_t parity, uint32_t abort_at,
+                                                 uint32_t* status) {
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_at(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      uint32_t aborted;
+      asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(aborted) : "r"(abort_at) : "memory");
+      if (aborted) return false;
+      if (it == (1u << 22)) {
+        asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(abort_at), "r"(1u) : "memory");
+        if (status) atomicOr(status, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// A reading warp's k-th unit (every lane takes part); false if a wait gave up.  TIMED: the MMA
+// warp's wait (mbar_wait); otherwise the softmax warps' (queue_wait_polls).
+template <int OFF, int ABORT, bool TIMED>
+__device__ __forceinline__ bool consume_unit(const AttnParams& p, int k, int lane, volatile int* abort_flag,
+                                             uint64_t budget, int& unit) {
+  if (!(p.deal & kDealDynamic)) {
+    unit = unit_of_round(p, k);
+    return true;
+  }
+  const uint32_t q = shared_at<OFF>();
+  const int s = k & (kUnitQ - 1);
+  const bool ready = TIMED ? mbar_wait_at(uq_full(q, s), (k / kUnitQ) & 1, abort_flag, p.status, budget)
+                           : queue_wait_polls(uq_full(q, s), (k / kUnitQ) & 1, shared_at<ABORT>(), p.status);
+  if (!__all_sync(0xffffffffu, ready)) return false;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(unit) : "r"(uq_slot(q, s)) : "memory");
+  __syncwarp();
+  if (lane == 0) mbar_arrive_at(uq_empty(q, s));
+  return true;
 }
 
 // Max over one row's 32 values of a 16x256b.x16 load (registers 4k + 2i + {0,1}, k < 16), then
@@ -263,6 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(&o_empty[i], kSoftmaxThreads);
     }
     mbar_init(mma_done, 1);
+    uint64_t* uq = reinterpret_cast<uint64_t*>(sm + L::kUnitQueue);
+    for (int i = 0; i < kUnitQ; ++i) {
+      mbar_init(uq + i, 1);                     // full: the producer's arrive
+      mbar_init(uq + kUnitQ + i, kUnitReaders);  // empty: one arrive per reading warp
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -279,10 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0, q_iter = 0;
       uint32_t kfills[STAGES], vfills[STAGES];
       for (int s = 0; s < STAGES; ++s) kfills[s] = vfills[s] = 0;
-      const int rounds = p.withhold_loads ? 0 : (p.n_units + gridDim.x - 1) / gridDim.x;
-      for (int t = 0; t < rounds; ++t) {
-        const int unit = unit_of_round(p, t);
-        if (unit >= p.n_units) continue;
+      for (int t = 0; !p.withhold_loads; ++t) {
+        int unit;
+        if (!produce_unit<L::kUnitQueue>(p, t, abort_flag, budget, unit) || unit >= p.n_units) break;
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
         const AttnSeg& s = *u.seg;
@@ -388,10 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ++gp[x];
         return true;
       };
-      const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
-      for (int t = 0; t < rounds && ok; ++t) {
-        const int unit = unit_of_round(p, t);
-        if (unit >= p.n_units) continue;
+      for (int t = 0; ok; ++t) {
+        int unit;
+        if (!consume_unit<L::kUnitQueue, L::kAbort, true>(p, t, lane, abort_flag, budget, unit) ||
+            unit >= p.n_units)
+          break;
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
         // Q and K/V come from TMA (async proxy, like the MMAs): the barrier waits order them, no
@@ -455,10 +552,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const bool r = mbar_wait(bar, parity, abort_flag, p.status, budget);
       return __all_sync(0xffffffffu, r);
     };
-    const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
-    for (int t = 0; t < rounds && ok; ++t) {
-      const int unit = unit_of_round(p, t);
-      if (unit >= p.n_units) continue;
+    for (int t = 0; ok; ++t) {
+      int unit;
+      if (!consume_unit<L::kUnitQueue, L::kAbort, false>(p, t, lane, abort_flag, budget, unit) ||
+          unit >= p.n_units)
+        break;
       const Unit u = decode_unit(p, unit);
       const AttnSeg& s = *u.seg;
       const int q0 = u.q0 + x * kAttnBM;  // first local row of this query tile
@@ -726,6 +824,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if ((p.deal & kDealDynamic) && threadIdx.x == 0) {
+    // Every role of this CTA is past its last take of a unit.  The last CTA to get here returns
+    // the counter (and this count of finished CTAs) to zero for the next launch.
+    __threadfence();
+    if (atomicAdd(p.counter + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.counter, 0u);
+      atomicExch(p.counter + 1, 0u);
+    }
+  }
 }
 
 template <int D, int STAGES, bool MASKS>
@@ -792,8 +899,19 @@ int deal_env() {
   return std::atoi(env) & (kDealCount - 1);
 }
 
+namespace {
+// The deals worth modelling: the static four and, with a counter, dynamic with either block order.
+constexpr int kDealChoices[] = {0, kDealRoundRobin, kDealAlternate, kDealRoundRobin | kDealAlternate,
+                                kDealDynamic, kDealDynamic | kDealAlternate};
+}  // namespace
+
 double deal_periods(const AttnParams& p, int deal, int ctas) {
   std::vector<double> load(ctas, 0.0), cost;
+  // dynamic: CTAs by (time free, index); the first free one takes the next unit
+  std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>,
+                      std::greater<std::pair<double, int>>> free_at;
+  if (deal & kDealDynamic)
+    for (int c = 0; c < ctas; ++c) free_at.push({0.0, c});
   for (int gi = 0; gi < p.n_groups; ++gi) {
     const AttnGroup& G = p.groups[gi];
     cost.clear();  // key tiles + epilogue of every block of the group, in block order
@@ -811,8 +929,15 @@ double deal_periods(const AttnParams& p, int deal, int ctas) {
     for (int i = 0; i < n; ++i) {
       const int unit = G.unit0 + i, t = unit / ctas;
       const int hb = i / G.blocks;
-      load[deal_unit(t, unit - t * ctas, ctas, deal) - t * ctas] +=
-          cost[deal_block(i - hb * G.blocks, G.blocks, hb, deal)];
+      const double c = cost[deal_block(i - hb * G.blocks, G.blocks, hb, deal)];
+      if (deal & kDealDynamic) {
+        const auto [at, cta] = free_at.top();
+        free_at.pop();
+        load[cta] = at + c;
+        free_at.push({at + c, cta});
+      } else {
+        load[deal_unit(t, unit - t * ctas, ctas, deal) - t * ctas] += c;
+      }
     }
   }
   return *std::max_element(load.begin(), load.end());
@@ -872,17 +997,19 @@ usp_status_t pack_attention(const AttnParams& base, std::vector<AttnSeg>& segs,
     p.n_segs = used;
     p.n_groups = n_groups;
     p.n_units = static_cast<int>(units);
-    // the unit deal with the shortest modelled launch, if it beats the default by more than 1 %
+    // the unit deal with the shortest modelled launch, if it beats the default by more than 0.5 %
     p.deal = 0;
+    const bool dynamic_ok = p.counter != nullptr;
     if (const int forced = deal_env(); forced >= 0) {
-      p.deal = forced;
+      p.deal = dynamic_ok ? forced : forced & ~kDealDynamic;
     } else if (units > 0) {
       const int ctas = std::max(1, std::min(p.n_units, sms > 0 ? sms : sm_count()));
       const double t0 = deal_periods(p, 0, ctas);
       double best = t0;
-      for (int d = 1; d < kDealCount; ++d) {
+      for (int d : kDealChoices) {
+        if (d == 0 || ((d & kDealDynamic) && !dynamic_ok)) continue;
         const double t = deal_periods(p, d, ctas);
-        if (t < best && t < 0.99 * t0) { best = t; p.deal = d; }
+        if (t < best && t < 0.995 * t0) { best = t; p.deal = d; }
       }
     }
     // the mask-free kernel when every link is whole key tiles without a causal diagonal

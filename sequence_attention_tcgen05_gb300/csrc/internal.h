@@ -176,10 +176,13 @@ struct AttnGroup {
 //   default: snake order (round t: CTA c takes unit t*G + c, or t*G + G-1-c for odd t), every
 //            (batch, head) visiting its blocks in the group's order (longest first);
 //   kDealRoundRobin: round t, CTA c takes unit t*G + c;
-//   kDealAlternate:  odd (batch, head) indices of a group visit their blocks in reverse order.
+//   kDealAlternate:  odd (batch, head) indices of a group visit their blocks in reverse order;
+//   kDealDynamic:    units in numbering order, each to the CTA that asks first (a counter in
+//                    global memory, AttnParams::counter); kDealRoundRobin has no effect then.
 constexpr int kDealRoundRobin = 1;
 constexpr int kDealAlternate = 2;
-constexpr int kDealCount = 4;
+constexpr int kDealDynamic = 4;
+constexpr int kDealCount = 8;
 // The unit CTA c takes in round t (the map is its own inverse within a round: the CTA that takes
 // unit u is deal_unit(u / G, u % G, G, deal) - (u / G) * G).
 __host__ __device__ inline int deal_unit(int t, int c, int G, int deal) {
@@ -200,7 +203,9 @@ struct AttnParams {
   int n_groups;
   int n_segs;
   int n_units;
-  int deal;            // kDealRoundRobin | kDealAlternate bits
+  int deal;            // kDealRoundRobin | kDealAlternate | kDealDynamic bits
+  // kDealDynamic: {next unit, finished CTAs}, zero at launch; the last CTA to finish zeroes both
+  uint32_t* counter;
   int B;
   float scale_log2;
   uint32_t* status;
@@ -232,16 +237,18 @@ struct AttnLaunch {
   bool masks;
 };
 // Packs the segments (sorted in place) and their links into launches, each starting from `base`
-// (maps, scale, status, budget), with the unit deal chosen for a grid of min(units, sms) CTAs
-// (sms = 0: the current device's SM count); run_attention runs them.
+// (maps, scale, status, budget, counter), with the unit deal chosen for a grid of
+// min(units, sms) CTAs (sms = 0: the current device's SM count; dynamic deals only with a
+// counter); run_attention runs them.
 usp_status_t pack_attention(const AttnParams& base, std::vector<AttnSeg>& segs,
                             const std::vector<AttnLink>& links, std::vector<AttnLaunch>& out,
                             int sms = 0);
 // Modelled time of one packed launch over `ctas` CTAs in key-tile periods under a unit deal: each
 // unit costs its key tiles plus an epilogue (2 periods for bf16 rows, 2.5 for fp32) and runs on
-// the CTA the deal gives it.  pack_attention gives each launch the deal with the shortest
-// modelled time when it beats the default by more than 1 %; USP_UNIT_DEAL=0..3 in the
-// environment (read at each call) forces one.
+// the CTA the deal gives it (dynamic: the CTA that becomes free first, the lowest index among
+// equals).  pack_attention gives each launch the deal with the shortest modelled time when it
+// beats the default by more than 0.5 %; USP_UNIT_DEAL=0..7 in the environment (read at each call)
+// forces one (a dynamic one falls back to its static bits without a counter).
 double deal_periods(const AttnParams& p, int deal, int ctas);
 int deal_env();  // -1 when USP_UNIT_DEAL is unset
 usp_status_t run_attention(const std::vector<AttnLaunch>& launches, int D, cudaStream_t stream);

@@ -292,10 +292,11 @@ def test_repeated_calls_on_the_same_buffers(monkeypatch):
 
 
 @pytest.mark.parametrize("B,S,H,D,U,R,causal,order,split,deal", [
-    (2, 1570, 3, 64, 1, 3, True, "zigzag", None, 1),       # round-robin beats the snake
-    (2, 600, 3, 64, 1, 4, True, "zigzag", None, 2),        # odd heads visit their blocks in reverse
+    (2, 1570, 4, 64, 1, 3, True, "zigzag", None, 1),       # round-robin beats the snake
+    (2, 2152, 2, 64, 1, 4, True, "zigzag", None, 2),       # odd heads visit their blocks in reverse
     (2, 1085, 3, 64, 1, 4, True, "contiguous", None, 3),   # both
-    (1, 3000, 16, 64, 1, 4, True, "stripe", None, 0),
+    (2, 600, 3, 64, 1, 4, True, "zigzag", None, 4),        # dynamic: the CTA free first
+    (1, 3000, 16, 64, 1, 4, True, "stripe", None, 4),
     (1, 2600, 16, 128, 2, 2, False, "contiguous", 2, 0),   # split fused ring: a second unit group
 ])
 @pytest.mark.parametrize("out", ["fp32", "bf16"])
@@ -311,7 +312,7 @@ def test_unit_deals_bit_identical(B, S, H, D, U, R, causal, order, split, deal, 
     chosen = usp.usp_plan_deals(B, S, H, D, causal, U, R, order, o_dt)
     assert [d for _, d, _, _ in chosen] == [deal] and chosen[0][0] > 152
     o, l, (qb, kb, vb) = run_usp(B, S, H, D, U, R, causal, order, seed=31, out=out)
-    for forced in range(4):
+    for forced in range(8):
         monkeypatch.setenv("USP_UNIT_DEAL", str(forced))
         assert [d for _, d, _, _ in usp.usp_plan_deals(B, S, H, D, causal, U, R, order, o_dt)] == \
             [forced] * len(chosen)
@@ -320,3 +321,51 @@ def test_unit_deals_bit_identical(B, S, H, D, U, R, causal, order, split, deal, 
         assert np.array_equal(l2.view(np.uint32), l.view(np.uint32)), forced
     ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), 1 / math.sqrt(D), causal)
     check_attention(o, l, ro, rl, f"deal {chosen} {order} causal={causal} out={out}")
+
+
+def test_dynamic_deal_counter(monkeypatch):
+    """The dynamic deal's counter (workspace bytes 8-15): four calls back to back on the same
+    buffers and workspace, with no host synchronisation between them (fresh inputs copied in
+    and each output copied out in the stream), each start from zero, left there by the launch
+    before (every output matches the oracle); a launch whose waits run out
+    (USP_TEST_WITHHOLD_LOADS: no unit is ever handed out) still leaves it at zero, and the next
+    call on the same workspace is correct."""
+    t = torch()
+    B, S, H, D, U, R = 2, 600, 3, 64, 1, 4
+    scale = 1 / math.sqrt(D)
+    monkeypatch.setenv("USP_UNIT_DEAL", "4")
+    assert [d for _, d, _, _ in usp.usp_plan_deals(B, S, H, D, True, U, R, "zigzag", usp.USP_FP32)] == [4]
+    nbytes = usp.usp_attention_workspace_size(B, S, H, D, U, R, "zigzag", usp.USP_FP32, True)
+    ws = t.zeros(nbytes, dtype=t.uint8, device="cuda")
+    ws[8:16] = 0x5A  # not zero: the first call with this workspace clears it in the stream
+    bits = [synth.make_qkv_bits(B, S, H, D, 40 + seed) for seed in range(4)]
+    dev = [tuple(to_dev_bf16(x) for x in b) for b in bits]
+    q, k, v = (t.empty_like(x) for x in dev[0])
+    o = t.empty((B, S, H, D), dtype=t.float32, device="cuda")
+    lse = t.empty((B, S, H), dtype=t.float32, device="cuda")
+    saved = []
+    t.cuda.synchronize()
+    for dq, dk, dv in dev:
+        q.copy_(dq)
+        k.copy_(dk)
+        v.copy_(dv)
+        usp.usp_attention(q, k, v, B, S, H, D, scale, True, U, R, o, lse, ws, nbytes, order="zigzag")
+        saved.append((o.clone(), lse.clone()))
+    assert usp.usp_check_status(ws) == usp.USP_OK
+    assert int(ws[8:16].view(t.int32).abs().sum()) == 0
+    for (qb, kb, vb), (so, sl) in zip(bits, saved):
+        ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), scale, True)
+        check_attention(so.cpu().numpy(), sl.cpu().numpy(), ro, rl, "dynamic deal, back to back")
+    monkeypatch.setenv("USP_WAIT_BUDGET_MS", "50")
+    monkeypatch.setenv("USP_TEST_WITHHOLD_LOADS", "1")
+    usp.usp_attention(q, k, v, B, S, H, D, scale, True, U, R, o, lse, ws, nbytes, order="zigzag")
+    assert usp.usp_check_status(ws) == usp.USP_ERR_TIMEOUT
+    assert int(ws[8:16].view(t.int32).abs().sum()) == 0
+    monkeypatch.delenv("USP_TEST_WITHHOLD_LOADS")
+    monkeypatch.delenv("USP_WAIT_BUDGET_MS")
+    o.fill_(0)
+    usp.usp_attention(q, k, v, B, S, H, D, scale, True, U, R, o, lse, ws, nbytes, order="zigzag")
+    assert usp.usp_check_status(ws) == usp.USP_OK
+    qb, kb, vb = bits[-1]
+    ro, rl = oracle.attention(widen(qb), widen(kb), widen(vb), scale, True)
+    check_attention(o.cpu().numpy(), lse.cpu().numpy(), ro, rl, "dynamic deal after a timed-out launch")
