@@ -67,8 +67,8 @@ SUSTAINED_MS = 250.0
 # dram__bytes_write.sum from one ncu capture of that workload's launch, with the hash of the kernel
 # code they were taken on (kernel_hash); reported as null once that code changes.
 ATTN_TRAFFIC = {
-    # one full-size launch: dram__bytes_read.sum 1698648064 + dram__bytes_write.sum 574548480
-    "llm_64k_ring8_zigzag": {"bytes": 1698648064 + 574548480, "kernel_hash": "98d4de6d55ab73fa"},
+    # one full-size launch: dram__bytes_read.sum 1697439744 + dram__bytes_write.sum 574841344
+    "llm_64k_ring8_zigzag": {"bytes": 1697439744 + 574841344, "kernel_hash": "75f1b74594938e16"},
 }
 L2_BYTES = 129e6
 

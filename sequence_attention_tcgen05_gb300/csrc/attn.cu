@@ -177,14 +177,10 @@ __device__ __forceinline__ uint32_t uq_full(uint32_t q, int s) { return q + 8 * 
 __device__ __forceinline__ uint32_t uq_empty(uint32_t q, int s) { return q + 8 * (kUnitQ + s); }
 __device__ __forceinline__ uint32_t uq_slot(uint32_t q, int s) { return q + 16 * kUnitQ + 4 * s; }
 
-// The producer thread's k-th unit; false if a wait gave up.
+// The producer thread's k-th unit under the dynamic deal; false if a wait gave up.
 template <int OFF>
 __device__ __forceinline__ bool produce_unit(const AttnParams& p, int k, volatile int* abort_flag,
                                              uint64_t budget, int& unit) {
-  if (!(p.deal & kDealDynamic)) {
-    unit = unit_of_round(p, k);
-    return true;
-  }
   const uint32_t q = shared_at<OFF>();
   const int s = k & (kUnitQ - 1);
   if (k >= kUnitQ && !mbar_wait_at(uq_empty(q, s), ((k / kUnitQ) - 1) & 1, abort_flag, p.status, budget))
@@ -219,15 +215,12 @@ __device__ __forceinline__ bool queue_wait_polls(uint32_t bar, uint32_t parity, 
   }
 }
 
-// A reading warp's k-th unit (every lane takes part); false if a wait gave up.  TIMED: the MMA
-// warp's wait (mbar_wait); otherwise the softmax warps' (queue_wait_polls).
+// A reading warp's k-th unit under the dynamic deal (every lane takes part); false if a wait
+// gave up.  TIMED: the MMA warp's wait (mbar_wait); otherwise the softmax warps'
+// (queue_wait_polls).
 template <int OFF, int ABORT, bool TIMED>
 __device__ __forceinline__ bool consume_unit(const AttnParams& p, int k, int lane, volatile int* abort_flag,
                                              uint64_t budget, int& unit) {
-  if (!(p.deal & kDealDynamic)) {
-    unit = unit_of_round(p, k);
-    return true;
-  }
   const uint32_t q = shared_at<OFF>();
   const int s = k & (kUnitQ - 1);
   const bool ready = TIMED ? mbar_wait_at(uq_full(q, s), (k / kUnitQ) & 1, abort_flag, p.status, budget)
@@ -312,8 +305,9 @@ __device__ __forceinline__ void quad_transpose4(uint32_t* w, int lane) {
 }
 
 // MASKS = false: the launch has no tile that needs a mask (every link whole key tiles, no causal
-// diagonal), so the kernel carries only the unmasked tile loop.
-template <int D, int STAGES, bool MASKS>
+// diagonal), so the kernel carries only the unmasked tile loop.  DYN: the launch deals its units
+// dynamically (kDealDynamic); the static deals' kernels carry no queue code.
+template <int D, int STAGES, bool MASKS, bool DYN>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using L = Layout<D, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -376,9 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0, q_iter = 0;
       uint32_t kfills[STAGES], vfills[STAGES];
       for (int s = 0; s < STAGES; ++s) kfills[s] = vfills[s] = 0;
-      for (int t = 0; !p.withhold_loads; ++t) {
+      // a static deal's CTA has `rounds` units or fewer; a dynamic one's walk ends at the first
+      // index past the last unit
+      const int rounds = p.withhold_loads ? 0 : (p.n_units + gridDim.x - 1) / gridDim.x;
+      for (int t = 0; DYN ? !p.withhold_loads : t < rounds; ++t) {
         int unit;
-        if (!produce_unit<L::kUnitQueue>(p, t, abort_flag, budget, unit) || unit >= p.n_units) break;
+        if constexpr (DYN) {
+          if (!produce_unit<L::kUnitQueue>(p, t, abort_flag, budget, unit) || unit >= p.n_units) break;
+        } else {
+          unit = unit_of_round(p, t);
+          if (unit >= p.n_units) continue;
+        }
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
         const AttnSeg& s = *u.seg;
@@ -484,11 +486,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ++gp[x];
         return true;
       };
-      for (int t = 0; ok; ++t) {
+      const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+      for (int t = 0; (DYN || t < rounds) && ok; ++t) {
         int unit;
-        if (!consume_unit<L::kUnitQueue, L::kAbort, true>(p, t, lane, abort_flag, budget, unit) ||
-            unit >= p.n_units)
-          break;
+        if constexpr (DYN) {
+          if (!consume_unit<L::kUnitQueue, L::kAbort, true>(p, t, lane, abort_flag, budget, unit) ||
+              unit >= p.n_units)
+            break;
+        } else {
+          unit = unit_of_round(p, t);
+          if (unit >= p.n_units) continue;
+        }
         const Unit u = decode_unit(p, unit);
         if (u.n_kv == 0) continue;
         // Q and K/V come from TMA (async proxy, like the MMAs): the barrier waits order them, no
@@ -552,11 +560,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const bool r = mbar_wait(bar, parity, abort_flag, p.status, budget);
       return __all_sync(0xffffffffu, r);
     };
-    for (int t = 0; ok; ++t) {
+    const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+    for (int t = 0; (DYN || t < rounds) && ok; ++t) {
       int unit;
-      if (!consume_unit<L::kUnitQueue, L::kAbort, false>(p, t, lane, abort_flag, budget, unit) ||
-          unit >= p.n_units)
-        break;
+      if constexpr (DYN) {
+        if (!consume_unit<L::kUnitQueue, L::kAbort, false>(p, t, lane, abort_flag, budget, unit) ||
+            unit >= p.n_units)
+          break;
+      } else {
+        unit = unit_of_round(p, t);
+        if (unit >= p.n_units) continue;
+      }
       const Unit u = decode_unit(p, unit);
       const AttnSeg& s = *u.seg;
       const int q0 = u.q0 + x * kAttnBM;  // first local row of this query tile
@@ -824,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if ((p.deal & kDealDynamic) && threadIdx.x == 0) {
+  if (DYN && threadIdx.x == 0) {
     // Every role of this CTA is past its last take of a unit.  The last CTA to get here returns
     // the counter (and this count of finished CTAs) to zero for the next launch.
     __threadfence();
@@ -835,11 +849,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   }
 }
 
-template <int D, int STAGES, bool MASKS>
+template <int D, int STAGES, bool MASKS, bool DYN>
 usp_status_t launch_one(const AttnParams& p, cudaStream_t stream) {
   using L = Layout<D, STAGES>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  auto kern = attn_fwd_kernel<D, STAGES, MASKS>;
+  auto kern = attn_fwd_kernel<D, STAGES, MASKS, DYN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return fail(USP_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   const int grid = std::max(1, std::min(p.n_units, sm_count()));
@@ -1024,8 +1038,14 @@ usp_status_t pack_attention(const AttnParams& base, std::vector<AttnSeg>& segs,
 usp_status_t run_attention(const std::vector<AttnLaunch>& launches, int D, cudaStream_t stream) {
   for (const AttnLaunch& L : launches) {
     const AttnParams& p = L.params;
-    usp_status_t st = D == 64 ? (L.masks ? launch_one<64, 4, true>(p, stream) : launch_one<64, 4, false>(p, stream))
-                              : (L.masks ? launch_one<128, 2, true>(p, stream) : launch_one<128, 2, false>(p, stream));
+    const bool dyn = (p.deal & kDealDynamic) != 0;
+    usp_status_t st;
+    if (D == 64)
+      st = L.masks ? (dyn ? launch_one<64, 4, true, true>(p, stream) : launch_one<64, 4, true, false>(p, stream))
+                   : (dyn ? launch_one<64, 4, false, true>(p, stream) : launch_one<64, 4, false, false>(p, stream));
+    else
+      st = L.masks ? (dyn ? launch_one<128, 2, true, true>(p, stream) : launch_one<128, 2, true, false>(p, stream))
+                   : (dyn ? launch_one<128, 2, false, true>(p, stream) : launch_one<128, 2, false, false>(p, stream));
     if (st != USP_OK) return st;
   }
   return USP_OK;
