@@ -6,9 +6,10 @@
 // step in ring order (the LSE-weighted merge done in registers) and writes the final O and LSE.
 //
 // Work units are numbered per unit group (one per Ulysses rank), head-major over the group's
-// segments (longest first), and dealt to the CTAs in a snake order: the longest units go first,
-// each CTA's total stays close to the mean, and CTAs running at the same time share one or two
-// heads' K/V in L2.
+// segments (longest first), so that CTAs running at the same time share one or two heads' K/V in
+// L2.  The host picks each launch's deal of units to CTAs from a time model: a static order
+// (snake or round-robin) that every role computes alone, or a dynamic one, where each CTA takes
+// the next unit from a counter in global memory when it is ready for one (the DYN kernels).
 //
 // One persistent CTA per SM, five warpgroups (640 threads):
 //   WG0  warp 0: TMA producer — the unit's two 128-row Q tiles, then K and V tiles into a
