@@ -363,3 +363,10 @@ def test_unit_deal_choices(L, monkeypatch):
     assert n == 432 and deal == 0 and t == t0
     with pytest.raises(usp.UspError):
         usp.usp_plan_deals(1, 65536, 32, 128, True, 1, 8, "zigzag", sms=0)
+    # the deal moves work between CTAs only: the workspace is the same under every forced deal
+    sizes = set()
+    for d in ("", "0", "3", "4", "6"):
+        monkeypatch.setenv("USP_UNIT_DEAL", d)
+        for args in ((1, 65793, 32, 128, 1, 8, "zigzag"), (1, 7145, 24, 128, 2, 2, "contiguous")):
+            sizes.add((args, usp.usp_attention_workspace_size(*args, usp.USP_BF16, True)))
+    assert len(sizes) == 2
