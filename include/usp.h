@@ -27,7 +27,7 @@
  *   - Errors are return codes; usp_last_error() gives a thread-local message for the last
  *     failing call of the calling thread.  Argument and workspace errors are found before
  *     anything is launched (except that usp_attention_noalloc has cleared its status word when
- *     a plan exceeds this build's limits); a CUDA error from a launch leaves the call's earlier
+ *     a plan exceeds this library's limits); a CUDA error from a launch leaves the call's earlier
  *     launches in the stream.
  *   - Stream order holds for every kernel.  The re-layout and merge kernels use programmatic
  *     dependent launch: they may be scheduled while the previous kernel of the stream drains,
@@ -50,7 +50,7 @@ typedef struct CUstream_st* usp_stream_t;
 typedef enum usp_status {
   USP_OK = 0,
   USP_ERR_INVALID_ARG = 1, /* bad size, split, pointer alignment or NULL pointer */
-  USP_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. D = 96) */
+  USP_ERR_UNSUPPORTED = 2, /* valid request this library does not implement (e.g. D = 96) */
   USP_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed (launch, tensor-map encode) */
   USP_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (from usp_check_status) */
   USP_ERR_WORKSPACE = 5,   /* workspace NULL, misaligned or smaller than required */
