@@ -276,7 +276,8 @@ def modelled_deal_periods(B, S, H, U, R, causal, order, bf16, deal, sms=152):
     visiting their 256-row blocks in order (causal: last block first), reversed for odd (batch,
     head) indices under deal & 2; a unit costs its key tiles + 2 (bf16 O) or 2.5 (fp32 O).  Under
     deal & 4 each unit in turn goes to the CTA free first (lowest index among equals); otherwise
-    unit i goes to CTA i % G in even rounds and, unless deal & 1, to G-1 - i % G in odd ones."""
+    unit i goes to CTA i % G in even rounds and, unless deal & 1, to G-1 - i % G in odd ones.
+    With sms=None: the unit costs in numbering order instead."""
     pieces = {}
     for (u, r, row0, rows, k, r2, kvlen, diag) in usp.usp_plan_chains(S, U, R, causal, order):
         pieces.setdefault((u, r, row0, rows), []).append((kvlen, diag))
@@ -300,6 +301,8 @@ def modelled_deal_periods(B, S, H, U, R, causal, order, bf16, deal, sms=152):
                 blocks.append(tiles(links, min(rows, 256 * (qb + 1)) - 1) + (2.0 if bf16 else 2.5))
         for hb in range(B * H // U):
             units += blocks[::-1] if (deal & 2) and hb % 2 else blocks
+    if sms is None:
+        return units
     ctas = min(len(units), sms)
     load = [0.0] * ctas
     if deal & 4:
@@ -342,6 +345,38 @@ def test_unit_deal_model(L, B, S, H, U, R, causal, order, monkeypatch):
             if want[d] < best and want[d] < 0.995 * want[0]:
                 pick, best = d, want[d]
         assert deal == pick and abs(t - want[deal]) < 1e-3
+
+
+def random_deal_cases(n, seed=7):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        U, R = int(rng.integers(1, 4)), int(rng.integers(1, 6))
+        H = U * int(rng.integers(1, 6))
+        S = int(rng.integers(max(U * R, 2), 9000))
+        out.append((int(rng.integers(1, 3)), S, H, U, R, bool(rng.integers(0, 2)),
+                    ["contiguous", "zigzag", "stripe"][int(rng.integers(0, 3))]))
+    return out
+
+
+@pytest.mark.parametrize("B,S,H,U,R,causal,order", random_deal_cases(16))
+def test_unit_deal_model_random_grids(L, B, S, H, U, R, causal, order, monkeypatch):
+    """The same restatement on random grids (sequence lengths that split unevenly, 1-5 ring
+    ranks, 1-3 Ulysses ranks, both batch sizes): every deal's modelled time matches, and none is
+    below the mean CTA's work (the sum of all unit costs over the CTAs)."""
+    monkeypatch.setenv("USP_RING_MERGE", "fused")
+    monkeypatch.setenv("USP_RING_SPLIT", "0")
+    for d in range(8):
+        monkeypatch.setenv("USP_UNIT_DEAL", str(d))
+        recs = usp.usp_plan_deals(B, S, H, 128, causal, U, R, order, usp.USP_BF16)
+        if len(recs) != 1:
+            continue  # more than one launch: the restatement covers one
+        ((n, deal, t, t0),) = recs
+        want = modelled_deal_periods(B, S, H, U, R, causal, order, True, d)
+        assert deal == d and abs(t - want) < 1e-3, (d, t, want)
+        units = modelled_deal_periods(B, S, H, U, R, causal, order, True, d, sms=None)
+        assert n == len(units)
+        assert t >= max(max(units), sum(units) / min(n, 152)) - 1e-6
 
 
 def test_unit_deal_choices(L, monkeypatch):
